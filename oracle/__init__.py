@@ -1,0 +1,251 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+This package is the slow, obviously-correct statement of what the CUDA
+library computes.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it.  It shares no code with the CUDA
+path and never imports the product package; it takes plain numpy arrays.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, one
+query row at a time from the definition).  This module only compiles it with
+gcc, marshals numpy arrays, and composes its steps:
+
+* :func:`forward` -- O, LSE and (optionally) the pre-softmax logits.
+* :func:`backward` -- exact dQ, dK, dV for every row (small shapes).
+* :func:`backward_sampled` -- dQ for chosen query rows and dK/dV for chosen
+  key rows, for shapes too large to do in full.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, special cases, finite differences, brute force on
+tiny inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+# Tests that plant a mistake in a copy of the C source point this at the
+# mutant's library (see tests/test_oracle_mutants.py).
+_LIB_OVERRIDE = os.environ.get("TATTN_ORACLE_LIB")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_ptr = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``_build/liboracle.so`` (gcc, OpenMP).
+
+    ``-ffp-contract=off`` keeps multiply and add separate so the x86 and Arm
+    builds round identically; no fast-math flags are used.
+    """
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC",
+               "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(_LIB_OVERRIDE or build())
+            lib.orc_set_threads.argtypes = [ctypes.c_int]
+            lib.orc_get_threads.restype = ctypes.c_int
+            lib.orc_fwd_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, _i64,
+                                         _dbl, ctypes.c_int, _ptr, _i64, _ptr, _ptr, _ptr]
+            lib.orc_delta_rows.argtypes = [_ptr, _ptr, _i64, _ptr, _i64, _ptr]
+            lib.orc_bwd_dq_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
+                                            _i64, _i64, _dbl, ctypes.c_int, _ptr, _i64, _ptr]
+            lib.orc_bwd_dkv_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
+                                             _i64, _i64, _dbl, ctypes.c_int, _ptr, _i64, _ptr,
+                                             _ptr]
+            _lib = lib
+    return _lib
+
+
+def set_threads(n: int) -> None:
+    _load().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().orc_get_threads())
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a) -> int | None:
+    return None if a is None else a.ctypes.data
+
+
+def _shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B,H,N,D]")
+    B, Hq, N, D = q.shape
+    Bk, Hkv, Nk, Dk = k.shape
+    if (Bk, Nk, Dk) != (B, N, D) or v.shape != k.shape or Hkv == 0 or Hq % Hkv:
+        raise ValueError(f"incompatible shapes q{q.shape} k{k.shape} v{v.shape}")
+    return B, Hq, Hkv, N, D
+
+
+def _rows(rows, total):
+    if rows is None:
+        return None, total
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    if r.size and (r.min() < 0 or r.max() >= total):
+        raise ValueError("row index out of range")
+    return r, int(r.size)
+
+
+def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
+            emit_logits: bool = False, logits_out=None):
+    """Exact attention forward in fp64.
+
+    q [B,Hq,N,D], k/v [B,Hkv,N,D] (any float dtype; widened to float64, which
+    holds bf16 and fp32 inputs exactly);
+    bias [B,Hq,N,N] or None (widened to float64).
+    rows: flat query-row indices ``(b*Hq + h)*N + i`` or None for all rows.
+
+    Returns dict with ``o`` ([B,Hq,N,D] when rows is None, else [nrows,D]),
+    ``lse`` (matching) and, when ``emit_logits``, ``logits`` ([B,Hq,N,N] or
+    [nrows,N]) holding s_ij for kept keys and NaN where the causal mask hides
+    the key.  ``logits_out`` may be given (float64, right shape) to reuse a
+    buffer; it may be the same array as ``bias`` when rows is None.
+    """
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, N, D = _shapes(q, k, v)
+    total = B * Hq * N
+    r, nrows = _rows(rows, total)
+    if bias is not None:
+        if not (isinstance(bias, np.ndarray) and bias.dtype == np.float64
+                and bias.flags.c_contiguous):
+            bias = _f64(bias)
+        if bias.shape != (B, Hq, N, N):
+            raise ValueError("bias must be [B,Hq,N,N]")
+    o = np.empty((nrows, D), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    logits = None
+    if emit_logits:
+        if logits_out is not None:
+            if (logits_out.dtype != np.float64 or not logits_out.flags.c_contiguous
+                    or logits_out.size != nrows * N):
+                raise ValueError("logits_out must be contiguous float64 of nrows*N")
+            if logits_out is bias and r is not None:
+                raise ValueError("logits_out may alias bias only for all rows")
+            logits = logits_out
+        else:
+            logits = np.empty((nrows, N), dtype=np.float64)
+    lib.orc_fwd_rows(_p(q), _p(k), _p(v), _p(bias), B, Hq, Hkv, N, D, float(scale),
+                     int(bool(causal)), _p(r), nrows, _p(o), _p(lse), _p(logits))
+    out = {}
+    if r is None:
+        out["o"] = o.reshape(B, Hq, N, D)
+        out["lse"] = lse.reshape(B, Hq, N)
+    else:
+        out["o"], out["lse"] = o, lse
+    if emit_logits:
+        if causal:
+            # Keys above the diagonal are not part of J_i: mark them NaN.
+            if r is None:
+                iu = np.triu_indices(N, 1)
+                for lg in logits.reshape(B * Hq, N, N):
+                    lg[iu] = np.nan
+            else:
+                lg = logits.reshape(nrows, N)
+                lg[np.arange(N)[None, :] > (r % N)[:, None]] = np.nan
+        out["logits"] = logits.reshape(B, Hq, N, N) if r is None else logits.reshape(nrows, N)
+    return out
+
+
+def delta(dO, o_rows, rows=None):
+    """Delta_i = sum_d dO_i[d] O_i[d] for the given rows (o_rows in row order)."""
+    lib = _load()
+    dO = _f64(dO)
+    D = dO.shape[-1]
+    o_rows = _f64(o_rows).reshape(-1, D)
+    r, nrows = _rows(rows, dO.size // D)
+    if o_rows.shape[0] != nrows:
+        raise ValueError("o_rows must hold one row per requested row")
+    out = np.empty((nrows,), dtype=np.float64)
+    lib.orc_delta_rows(_p(dO), _p(o_rows), D, _p(r), nrows, _p(out))
+    return out
+
+
+def backward(q, k, v, dO, *, scale: float, causal: bool):
+    """Exact dQ, dK, dV (fp64) for every row; returns dict with o, lse too."""
+    lib = _load()
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, N, D = _shapes(q, k, v)
+    fw = forward(q, k, v, scale=scale, causal=causal)
+    lse = np.ascontiguousarray(fw["lse"].reshape(-1))
+    dlt = delta(dO, fw["o"].reshape(-1, D))
+    dq = np.empty((B * Hq * N, D), dtype=np.float64)
+    dk = np.empty((B * Hkv * N, D), dtype=np.float64)
+    dv = np.empty((B * Hkv * N, D), dtype=np.float64)
+    lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
+                        float(scale), int(bool(causal)), None, B * Hq * N, _p(dq))
+    lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
+                         float(scale), int(bool(causal)), None, B * Hkv * N, _p(dk), _p(dv))
+    return {"o": fw["o"], "lse": fw["lse"], "dq": dq.reshape(B, Hq, N, D),
+            "dk": dk.reshape(B, Hkv, N, D), "dv": dv.reshape(B, Hkv, N, D)}
+
+
+def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows):
+    """dQ at flat query rows ``q_rows`` and dK/dV at flat key rows ``k_rows``.
+
+    Key row flat index is ``(b*Hkv + g)*N + j``.  The statistics LSE and Delta
+    are computed by the oracle's own forward pass over every query row of the
+    heads involved (a key row needs all the query rows that attend to it).
+    Returns dict with dq [len(q_rows), D], dk and dv [len(k_rows), D].
+    """
+    lib = _load()
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, N, D = _shapes(q, k, v)
+    group = Hq // Hkv
+    qr, nq = _rows(q_rows, B * Hq * N)
+    kr, nk = _rows(k_rows, B * Hkv * N)
+    # Query rows whose statistics are needed.
+    need = set() if qr is None else {int(x) for x in qr}
+    heads = set()
+    for x in (kr if kr is not None else []):
+        bg = int(x) // N
+        b, g = divmod(bg, Hkv)
+        for h in range(g * group, (g + 1) * group):
+            heads.add(b * Hq + h)
+    stat_rows = sorted(need | {bh * N + i for bh in heads for i in range(N)}
+                       if heads else need)
+    stat_rows = np.asarray(stat_rows, dtype=np.int64)
+    lse = np.zeros((B * Hq * N,), dtype=np.float64)
+    dlt = np.zeros((B * Hq * N,), dtype=np.float64)
+    if stat_rows.size:
+        fw = forward(q, k, v, scale=scale, causal=causal, rows=stat_rows)
+        lse[stat_rows] = fw["lse"]
+        dlt[stat_rows] = delta(dO, fw["o"], stat_rows)
+    dq = np.empty((nq, D), dtype=np.float64)
+    dk = np.empty((nk, D), dtype=np.float64)
+    dv = np.empty((nk, D), dtype=np.float64)
+    if nq:
+        lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
+                            float(scale), int(bool(causal)), _p(qr), nq, _p(dq))
+    if nk:
+        lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
+                             float(scale), int(bool(causal)), _p(kr), nk, _p(dk), _p(dv))
+    return {"dq": dq, "dk": dk, "dv": dv}
