@@ -1,0 +1,158 @@
+/*
+ * tattn.h -- C ABI of the tiled exact-attention library for GB300 (sm_103a).
+ *
+ * The library computes exact attention
+ *
+ *     O = softmax(scale * Q K^T  [+ bias]  [+ causal mask]) V
+ *
+ * tile by tile with an online softmax, so that the N x N score and
+ * probability matrices never reach device memory, and saves one fp32
+ * log-sum-exp per query row for a backward pass that recomputes the
+ * probabilities from it.
+ *
+ * Sources of the operations (page title and section):
+ *  - Standard attention S = QK^T / sqrt(d), P = softmax(S), O = PV and the
+ *    N x N intermediates it materialises: "FlashAttention原理与Triton实战：
+ *    突破Attention显存瓶颈", sections 1 and 2.1; kwkr.cn/news/592482, 1.1.
+ *  - Online softmax block merge (m_new = max(m_old, m_blk), alpha =
+ *    exp(m_old - m_new), l and O rescaled by alpha, divide by l at the end)
+ *    and the tiled double loop: kwkr.cn/news/592482, 2.2 and 2.3.
+ *  - Causal mask (key j kept for query i iff j <= i): kwkr.cn/news/592482,
+ *    3.3 and 3.4; blog.ans20xx.com/posts/ai/day26, "最小 attention wrapper".
+ *  - Additive pre-softmax logit bias read from the previous layer and the
+ *    logits emitted for the next layer (block attention residual):
+ *    Block Attention Residual Triton kernel (iqiancheng.github.io), sections
+ *    "Block Attention Residual 做了什么" and "v1: Fuse Residual 进 Attention
+ *    Kernel", "v2: 优化 torch.cat + SRAM 复用".
+ *  - Backward by recomputation from saved row statistics:
+ *    kwkr.cn/news/592482, 2.4; "FlashAttention原理与Triton实战", 2.3 and 4.3.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are dense, contiguous, row-major:
+ *      q, o, dO, dq : bf16 [B, Hq,  N, D]
+ *      k, v, dk, dv : bf16 [B, Hkv, N, D]
+ *      lse          : fp32 [B, Hq,  N]
+ *      bias, logits : fp32 [B, Hq,  N, N]
+ *  - Grouped heads: query head h reads key/value head h / (Hq / Hkv);
+ *    Hq must be a multiple of Hkv (Hkv == Hq is plain multi-head).
+ *  - D must be 64 or 128.  N, B, Hq, Hkv are any positive sizes (N need not
+ *    be a multiple of the 128-row tile); a zero size is an empty problem and
+ *    returns ATTN_OK without launching anything.
+ *  - Every tensor pointer is a DEVICE pointer of the current CUDA device,
+ *    owned by the caller; bf16 tensors must be 16-byte aligned, fp32 tensors
+ *    4-byte aligned.  The library allocates no device memory for its
+ *    kernels; the backward takes its scratch from a caller-provided
+ *    workspace.  The only device state is one small status word per device.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous and stream-ordered: they return after
+ *    the launches are queued.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns ATTN_ERR_INVALID (or ATTN_ERR_UNSUPPORTED for a valid
+ *    but unimplemented case) and touches no memory.  A launch failure
+ *    returns ATTN_ERR_CUDA.  Faults found on the device (a pipeline wait
+ *    that ran out of time, a failed device-side check) do not trap: the
+ *    kernel records a code in the status word and returns; read it with
+ *    attn_last_device_status().
+ */
+#ifndef TATTN_H
+#define TATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,      /* null/misaligned pointer, bad size or shape      */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid request outside what is implemented       */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed               */
+    ATTN_ERR_TIMEOUT = 4,      /* a device pipeline wait exceeded its time limit  */
+    ATTN_ERR_DEVICE_CHECK = 5  /* a device-side consistency check failed          */
+} attn_status;
+
+/*
+ * Forward pass.
+ *
+ *   q            bf16 [B,Hq,N,D]   queries                          (in)
+ *   k, v         bf16 [B,Hkv,N,D]  keys, values                     (in)
+ *   bias         fp32 [B,Hq,N,N]   additive logit bias, or NULL     (in)
+ *                Added, unscaled, to scale*QK^T before the mask and the
+ *                softmax (the previous layer's pre-softmax logits in a
+ *                block attention residual).  Under the causal mask only
+ *                entries with j <= i are read.
+ *   o            bf16 [B,Hq,N,D]   output, rounded to nearest even  (out)
+ *   lse          fp32 [B,Hq,N]     LSE_i = m_i + ln l_i over the scaled,
+ *                biased, masked logits (natural log), or NULL       (out)
+ *   scale        multiplier of QK^T (usually 1/sqrt(D)); must be finite.
+ *   causal       nonzero: key j is kept for query i iff j <= i.
+ *   emit_logits  fp32 [B,Hq,N,N] or NULL                            (out)
+ *                Receives s_ij = scale*q_i.k_j + bias_ij (bias term absent
+ *                when bias is NULL) for every kept entry; under the causal
+ *                mask, tiles strictly above the diagonal are not written and
+ *                masked entries inside diagonal tiles hold unspecified
+ *                values.  MAY be the same pointer as bias (in-place update
+ *                of a preallocated residual buffer): each bias element is
+ *                read by the only thread block that later overwrites it.
+ *                Any other overlap between outputs and inputs is invalid.
+ *
+ * Returns ATTN_OK once the kernel is queued on `stream`.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, const float *bias,
+                     void *o, float *lse,
+                     int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                     float *emit_logits, void *stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this shape (fp32 dQ
+ * accumulator [B,Hq,N,D] and fp32 Delta [B,Hq,N], each rounded up to 256
+ * bytes).  Returns 0 for an empty problem or invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D);
+
+/*
+ * Backward pass by recomputation (no bias; the forward must have been run
+ * without bias on the same q, k, v, scale and causal setting).
+ *
+ *   q, k, v      as for attn_fwd                                    (in)
+ *   o            bf16 [B,Hq,N,D]  forward output                    (in)
+ *   lse          fp32 [B,Hq,N]    forward log-sum-exp               (in)
+ *   dO           bf16 [B,Hq,N,D]  gradient of the loss w.r.t. O     (in)
+ *   dq           bf16 [B,Hq,N,D]                                    (out)
+ *   dk, dv       bf16 [B,Hkv,N,D] (summed over each kv head's query
+ *                heads when Hq > Hkv)                               (out)
+ *   workspace    device scratch of at least attn_bwd_workspace_size()
+ *                bytes, 256-byte aligned, owned by the caller; its contents
+ *                on entry do not matter and are clobbered.
+ *
+ * Computes P_ij = exp(scale q_i.k_j - LSE_i), dV = P^T dO, dP = dO V^T,
+ * Delta_i = sum_d dO_id O_id, dS = P o (dP - Delta), dQ = scale dS K,
+ * dK = scale dS^T Q.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const void *dO,
+                     void *dq, void *dk, void *dv,
+                     int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *attn_status_string(attn_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns ATTN_OK if no kernel since the last call recorded a fault,
+ * else the first code recorded (ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_CHECK), or
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status attn_last_device_status(void *stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TATTN_H */

@@ -68,7 +68,8 @@ def _load():
             lib.orc_set_threads.argtypes = [ctypes.c_int]
             lib.orc_get_threads.restype = ctypes.c_int
             lib.orc_fwd_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, _i64,
-                                         _dbl, ctypes.c_int, _ptr, _i64, _ptr, _ptr, _ptr]
+                                         _dbl, ctypes.c_int, _ptr, _i64, ctypes.c_int, _ptr,
+                                         _ptr, _ptr]
             lib.orc_delta_rows.argtypes = [_ptr, _ptr, _i64, _ptr, _i64, _ptr]
             lib.orc_bwd_dq_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
                                             _i64, _i64, _dbl, ctypes.c_int, _ptr, _i64, _ptr]
@@ -120,7 +121,8 @@ def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
 
     q [B,Hq,N,D], k/v [B,Hkv,N,D] (any float dtype; widened to float64, which
     holds bf16 and fp32 inputs exactly);
-    bias [B,Hq,N,N] or None (widened to float64).
+    bias [B,Hq,N,N] or None (widened to float64); with ``rows`` given, bias
+    may instead be [nrows, N]: the bias rows of the requested rows only.
     rows: flat query-row indices ``(b*Hq + h)*N + i`` or None for all rows.
 
     Returns dict with ``o`` ([B,Hq,N,D] when rows is None, else [nrows,D]),
@@ -138,8 +140,11 @@ def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
         if not (isinstance(bias, np.ndarray) and bias.dtype == np.float64
                 and bias.flags.c_contiguous):
             bias = _f64(bias)
-        if bias.shape != (B, Hq, N, N):
-            raise ValueError("bias must be [B,Hq,N,N]")
+        per_request = r is not None and bias.shape == (nrows, N)
+        if bias.shape != (B, Hq, N, N) and not per_request:
+            raise ValueError("bias must be [B,Hq,N,N] (or [nrows,N] with rows)")
+    else:
+        per_request = False
     o = np.empty((nrows, D), dtype=np.float64)
     lse = np.empty((nrows,), dtype=np.float64)
     logits = None
@@ -148,13 +153,14 @@ def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
             if (logits_out.dtype != np.float64 or not logits_out.flags.c_contiguous
                     or logits_out.size != nrows * N):
                 raise ValueError("logits_out must be contiguous float64 of nrows*N")
-            if logits_out is bias and r is not None:
-                raise ValueError("logits_out may alias bias only for all rows")
+            if logits_out is bias and r is not None and not per_request:
+                raise ValueError("logits_out may alias a full bias only for all rows")
             logits = logits_out
         else:
             logits = np.empty((nrows, N), dtype=np.float64)
     lib.orc_fwd_rows(_p(q), _p(k), _p(v), _p(bias), B, Hq, Hkv, N, D, float(scale),
-                     int(bool(causal)), _p(r), nrows, _p(o), _p(lse), _p(logits))
+                     int(bool(causal)), _p(r), nrows, int(per_request), _p(o), _p(lse),
+                     _p(logits))
     out = {}
     if r is None:
         out["o"] = o.reshape(B, Hq, N, D)
@@ -224,15 +230,18 @@ def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows)
     kr, nk = _rows(k_rows, B * Hkv * N)
     # Query rows whose statistics are needed.
     need = set() if qr is None else {int(x) for x in qr}
-    heads = set()
+    # A key row j of kv head (b, g) needs every query row of the group's
+    # heads that attends to it: i >= j under the causal mask, all i otherwise.
+    first = {}
     for x in (kr if kr is not None else []):
-        bg = int(x) // N
+        bg, j = divmod(int(x), N)
         b, g = divmod(bg, Hkv)
+        lo = j if causal else 0
         for h in range(g * group, (g + 1) * group):
-            heads.add(b * Hq + h)
-    stat_rows = sorted(need | {bh * N + i for bh in heads for i in range(N)}
-                       if heads else need)
-    stat_rows = np.asarray(stat_rows, dtype=np.int64)
+            first[b * Hq + h] = min(first.get(b * Hq + h, N), lo)
+    for bh, lo in first.items():
+        need |= set(range(bh * N + lo, bh * N + N))
+    stat_rows = np.asarray(sorted(need), dtype=np.int64)
     lse = np.zeros((B * Hq * N,), dtype=np.float64)
     dlt = np.zeros((B * Hq * N,), dtype=np.float64)
     if stat_rows.size:

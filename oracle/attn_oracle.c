@@ -115,14 +115,17 @@ static void row_stats(const double *s, int64_t nk, double *m_out, double *l_out)
  *   o      [nrows, D]  output rows O_i
  *   lse    [nrows]     LSE_i = m_i + ln l_i (may be NULL)
  *   logits [nrows, N]  s_ij for j in J_i; other entries left as they were
- *                      (may be NULL). May alias bias only when rows is NULL
- *                      (then request order is the natural row order).
- * rows == NULL means every row, in natural order.
+ *                      (may be NULL). May alias bias when the bias rows are
+ *                      read in request order (each row reads its bias before
+ *                      writing its logits).
+ * rows == NULL means every row, in natural order.  bias is [B,Hq,N,N]
+ * indexed by the flat row, or, when bias_per_request is nonzero, [nrows, N]
+ * indexed by request (the bias rows of the requested rows only).
  */
 void orc_fwd_rows(const double *q, const double *k, const double *v, const double *bias,
                   int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t D,
                   double scale, int causal, const int64_t *rows, int64_t nrows,
-                  double *o, double *lse, double *logits)
+                  int bias_per_request, double *o, double *lse, double *logits)
 {
     (void)B;
     const int64_t group = Hq / Hkv;
@@ -139,7 +142,7 @@ void orc_fwd_rows(const double *q, const double *k, const double *v, const doubl
             const double *q_row = q + flat * D;
             const double *k_head = k + (b * Hkv + g) * N * D;
             const double *v_head = v + (b * Hkv + g) * N * D;
-            const double *bias_row = bias ? bias + flat * N : NULL;
+            const double *bias_row = bias ? bias + (bias_per_request ? r : flat) * N : NULL;
             const int64_t nk = key_count(i, N, causal);
 
             row_logits(q_row, k_head, bias_row, nk, D, scale, s);

@@ -1,0 +1,96 @@
+"""Host-only checks of the C ABI: the library loads, exports every entry
+point include/tattn.h declares, and rejects bad arguments before touching
+any memory (no GPU needed: invalid calls return before any CUDA call)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ta():
+    import tiled_attention_02_gb300 as ta
+    ta.build()
+    return ta
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(attn_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_entry_points():
+    assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string",
+            "attn_last_device_status"} <= declared_functions()
+
+
+def test_library_exports_every_declared_symbol(ta):
+    L = ta.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(ta.EXPORTED) == declared_functions()
+
+
+def test_status_strings(ta):
+    for code in range(6):
+        s = ta.attn_status_string(code)
+        assert s.startswith("ATTN_")
+    assert "unknown" in ta.attn_status_string(99)
+
+
+A = 0x10000   # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def fwd(ta, **kw):
+    args = dict(q=A, k=A, v=A, bias=None, o=A, lse=None, B=1, Hq=2, Hkv=1, N=256, D=128,
+                scale=0.125, causal=0, emit=None, stream=None)
+    args.update(kw)
+    return ta.raw_attn_fwd(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1),
+    (dict(q=A + 2), 1), (dict(k=A + 8), 1), (dict(o=A + 4), 1),
+    (dict(bias=A + 2), 1), (dict(emit=A + 1), 1), (dict(lse=A + 3), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(D=0), 1), (dict(D=-64), 1),
+    (dict(Hkv=3), 1), (dict(Hkv=0), 1), (dict(B=-1), 1), (dict(N=-5), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+])
+def test_fwd_rejects_bad_arguments(ta, kw, code):
+    assert fwd(ta, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=0), dict(N=0), dict(B=0, q=None)])
+def test_fwd_empty_problem_is_ok_without_launch(ta, kw):
+    assert fwd(ta, **kw) == 0
+
+
+def bwd(ta, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, do=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=2, N=256,
+                D=64, scale=0.125, causal=1, ws=A, ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    return ta.raw_attn_bwd(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lse=None), 1), (dict(do=None), 1), (dict(ws=None), 1), (dict(dk=A + 2), 1),
+    (dict(ws=A + 16), 1), (dict(ws_bytes=1000), 1), (dict(D=32), 2), (dict(Hkv=3), 1),
+])
+def test_bwd_rejects_bad_arguments(ta, kw, code):
+    assert bwd(ta, **kw) == code
+
+
+def test_workspace_size(ta):
+    # fp32 dQ accumulator + fp32 Delta, each rounded up to 256 bytes
+    assert ta.attn_bwd_workspace_size(1, 16, 16, 16384, 128) == 16 * 16384 * 128 * 4 + 16 * 16384 * 4
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 64) == 768 + 256
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 5, 64) == 1280 + 256
+    assert ta.attn_bwd_workspace_size(0, 1, 1, 3, 64) == 0
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 96) == 0

@@ -16,6 +16,7 @@ SRC = os.path.join(ROOT, "oracle", "attn_oracle.c")
 # (name, original text, planted mistake)
 MUTANTS = [
     ("dropped_scale", "s[j] = scale * dot + (bias_row", "s[j] = dot + (bias_row"),
+    ("bias_wrong_row", "bias + (bias_per_request ? r : flat) * N", "bias + (bias_per_request ? r : flat) * N + 1"),
     ("bias_scaled", "s[j] = scale * dot + (bias_row ? bias_row[j] : 0.0);",
      "s[j] = scale * (dot + (bias_row ? bias_row[j] : 0.0));"),
     ("causal_excludes_diagonal", "return causal ? i + 1 : N;", "return causal ? i : N;"),

@@ -377,3 +377,21 @@ def test_backward_zero_output_grad(orc):
     g = orc.backward(q, k, v, np.zeros((B, H, N, D)), scale=0.5, causal=True)
     for name in ("dq", "dk", "dv"):
         assert np.abs(g[name]).max() == 0.0
+
+
+def test_per_request_bias_rows_equal_full_bias(orc):
+    """Sampled rows with only their own bias rows give the same result as the
+    full bias, and a block chain can be followed row by row (row i of S_L
+    depends only on row i of S_{L-1})."""
+    B, Hq, Hkv, N, D = 1, 4, 2, 7, 3
+    bias = rand(B, Hq, N, N)
+    rows = np.array([1, 8, 27])
+    layers = [(rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D)) for _ in range(3)]
+    full_bias, part_bias = bias.copy(), bias.reshape(-1, N)[rows].copy()
+    for q, k, v in layers:
+        f = orc.forward(q, k, v, scale=0.5, causal=True, bias=full_bias, emit_logits=True)
+        p = orc.forward(q, k, v, scale=0.5, causal=True, bias=part_bias, rows=rows,
+                        emit_logits=True, logits_out=part_bias)
+        np.testing.assert_array_equal(p["o"], f["o"].reshape(-1, D)[rows])
+        np.testing.assert_array_equal(p["logits"], f["logits"].reshape(-1, N)[rows])
+        full_bias = f["logits"]

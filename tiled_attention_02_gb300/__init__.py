@@ -1,0 +1,191 @@
+"""tiled_attention_02_gb300 -- Python binding of the tiled exact-attention
+C library for GB300 (sm_103a).
+
+Every step of the computation runs in the library's CUDA kernels; this
+module only marshals arguments (device pointers of PyTorch tensors, sizes,
+the current CUDA stream) into the C ABI declared in ``include/tattn.h`` and
+turns a non-OK status into an exception.  There is no CPU or PyTorch
+fallback: if the library is missing the calls raise.
+
+Functions mirror the C entry points:
+
+* :func:`attn_fwd` -- ``attn_fwd`` (O, LSE, optional bias in / logits out)
+* :func:`attn_bwd` -- ``attn_bwd`` (dQ, dK, dV by recomputation)
+* :func:`attn_bwd_workspace_size`, :func:`attn_last_device_status`,
+  :func:`attn_status_string`
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_DEVICE_CHECK = 5
+
+# Every symbol include/tattn.h declares.
+EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
+            "attn_last_device_status", "attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"tattn CUDA library not built: {LIB_PATH} is missing "
+                                   "(run tiled_attention_02_gb300.build())")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]
+            L.attn_fwd.restype = i
+            L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+            L.attn_bwd_workspace_size.restype = sz
+            L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                   sz, vp]
+            L.attn_bwd.restype = i
+            L.attn_status_string.argtypes = [i]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_last_device_status.argtypes = [vp]
+            L.attn_last_device_status.restype = i
+            L.attn_version.argtypes = []
+            L.attn_version.restype = i
+            _lib = L
+    return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, dtype, shape):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def raw_attn_fwd(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, scale, causal, emit, stream) -> int:
+    """The C entry point with raw integer pointers; returns the status code."""
+    return lib().attn_fwd(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, ctypes.c_float(scale),
+                          int(causal), emit, stream)
+
+
+def raw_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal, ws,
+                 ws_bytes, stream) -> int:
+    return lib().attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D,
+                          ctypes.c_float(scale), int(causal), ws, ws_bytes, stream)
+
+
+def attn_fwd(q, k, v, bias=None, *, scale: float | None = None, causal: bool = False,
+             o=None, lse=None, emit_logits=None, want_lse: bool = True, stream=None):
+    """Exact attention forward through the C ABI.
+
+    q [B,Hq,N,D], k/v [B,Hkv,N,D] bf16 CUDA tensors; bias (optional) fp32
+    [B,Hq,N,N]; emit_logits (optional) fp32 [B,Hq,N,N] output buffer, which
+    may be ``bias`` itself.  Returns ``(o, lse)`` (lse is None when
+    ``want_lse`` is False and no ``lse`` buffer is given).
+    """
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    _check(q, "q", torch.bfloat16, (B, Hq, N, D))
+    _check(k, "k", torch.bfloat16, (B, Hkv, N, D))
+    _check(v, "v", torch.bfloat16, (B, Hkv, N, D))
+    _check(bias, "bias", torch.float32, (B, Hq, N, N))
+    _check(emit_logits, "emit_logits", torch.float32, (B, Hq, N, N))
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", torch.bfloat16, (B, Hq, N, D))
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _check(lse, "lse", torch.float32, (B, Hq, N))
+    st = raw_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(lse), B, Hq, Hkv, N,
+                      D, scale, causal, _ptr(emit_logits), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, D: int) -> int:
+    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, N, D))
+
+
+def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = False,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward by recomputation through the C ABI; returns (dq, dk, dv)."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    for t, name, dt, shp in ((q, "q", torch.bfloat16, (B, Hq, N, D)),
+                             (k, "k", torch.bfloat16, (B, Hkv, N, D)),
+                             (v, "v", torch.bfloat16, (B, Hkv, N, D)),
+                             (o, "o", torch.bfloat16, (B, Hq, N, D)),
+                             (lse, "lse", torch.float32, (B, Hq, N)),
+                             (do, "do", torch.bfloat16, (B, Hq, N, D))):
+        _check(t, name, dt, shp)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = attn_bwd_workspace_size(B, Hq, Hkv, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = raw_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                      _ptr(dk), _ptr(dv), B, Hq, Hkv, N, D, scale, causal, _ptr(workspace),
+                      workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_last_device_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the device status word."""
+    return int(lib().attn_last_device_status(_stream_handle(stream)))

@@ -1,0 +1,212 @@
+// attn_api.cu -- the C ABI declared in include/tattn.h: argument checks,
+// TMA tensor-map encoding, the per-device status word, and dispatch to the
+// kernel launchers.
+#include <math.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "tattn.h"
+
+namespace tattn {
+namespace {
+
+// One status word per device; a kernel that meets a fault records the first
+// code here instead of trapping.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common size checks.  Returns ATTN_OK, or the code to return; sets *empty
+// when there is nothing to compute.
+attn_status check_sizes(int B, int Hq, int Hkv, int N, int D, float scale, bool *empty) {
+    *empty = false;
+    if (B < 0 || Hq < 0 || Hkv < 0 || N < 0) return ATTN_ERR_INVALID;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID;
+    if (D != 64 && D != 128) return (D > 0) ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID;
+    if (B == 0 || Hq == 0 || N == 0) {
+        *empty = true;
+        return ATTN_OK;
+    }
+    if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    // Tile and head indices are 32-bit in the kernels; element offsets 64-bit.
+    const long long BH = static_cast<long long>(B) * Hq;
+    const long long ntiles = (static_cast<long long>(N) + 127) / 128;
+    if (BH * ntiles > 0x7fffffffLL || BH > 0xffffffffLL) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+bool encode_bf16_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
+                      int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(heads)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int *device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+}  // namespace tattn
+
+using namespace tattn;
+
+extern "C" {
+
+attn_status attn_fwd(const void *q, const void *k, const void *v, const float *bias, void *o,
+                     float *lse, int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                     float *emit_logits, void *stream) {
+    bool empty = false;
+    attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return ATTN_ERR_INVALID;
+    if ((bias && !aligned(bias, 4)) || (emit_logits && !aligned(emit_logits, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return ATTN_ERR_INVALID;
+    if (bias || emit_logits) {
+        // [B,Hq,N,N] element offsets must fit in 64 bits.
+        const double elems = static_cast<double>(B) * Hq * static_cast<double>(N) * N;
+        if (elems > 9.0e18) return ATTN_ERR_UNSUPPORTED;
+    }
+    FwdProblem pb;
+    pb.q = q;
+    pb.k = k;
+    pb.v = v;
+    pb.bias = bias;
+    pb.o = o;
+    pb.lse = lse;
+    pb.emit = emit_logits;
+    pb.B = B;
+    pb.Hq = Hq;
+    pb.Hkv = Hkv;
+    pb.N = N;
+    pb.D = D;
+    pb.scale = scale;
+    pb.causal = causal != 0;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    cudaError_t e = launch_fwd(pb, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D) {
+    bool empty = false;
+    if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
+    auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    return round256(rows * D * sizeof(float)) + round256(rows * sizeof(float));
+}
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N,
+                     int D, float scale, int causal, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    bool empty = false;
+    attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+        return ATTN_ERR_INVALID;
+    const void *bf[] = {q, k, v, o, dO, dq, dk, dv};
+    for (const void *p : bf)
+        if (!aligned(p, 16)) return ATTN_ERR_INVALID;
+    if (!aligned(lse, 4) || !aligned(workspace, 256)) return ATTN_ERR_INVALID;
+    const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, N, D);
+    if (workspace_bytes < need) return ATTN_ERR_INVALID;
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    const size_t acc_bytes = (rows * D * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    BwdProblem pb;
+    pb.q = q;
+    pb.k = k;
+    pb.v = v;
+    pb.o = o;
+    pb.dO = dO;
+    pb.lse = lse;
+    pb.dq = dq;
+    pb.dk = dk;
+    pb.dv = dv;
+    pb.B = B;
+    pb.Hq = Hq;
+    pb.Hkv = Hkv;
+    pb.N = N;
+    pb.D = D;
+    pb.scale = scale;
+    pb.causal = causal != 0;
+    pb.dq_acc = static_cast<float *>(workspace);
+    pb.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc_bytes);
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    cudaError_t e = launch_bwd(pb, status, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+const char *attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID: return "ATTN_ERR_INVALID: invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: valid but unsupported request";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA call failed";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a device pipeline wait timed out";
+        case ATTN_ERR_DEVICE_CHECK: return "ATTN_ERR_DEVICE_CHECK: a device-side check failed";
+    }
+    return "unknown attn_status";
+}
+
+attn_status attn_last_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    int *p = device_status_ptr();
+    if (!p) return ATTN_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (h != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    return static_cast<attn_status>(h);
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

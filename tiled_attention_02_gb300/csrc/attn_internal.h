@@ -1,0 +1,48 @@
+// attn_internal.h -- host-side interface between the C-ABI layer and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tattn {
+
+// Validated forward problem (device pointers, sizes in elements).
+struct FwdProblem {
+    const void *q, *k, *v;
+    const float *bias;
+    void *o;
+    float *lse;
+    float *emit;
+    int B, Hq, Hkv, N, D;
+    float scale;
+    bool causal;
+};
+
+// Validated backward problem.
+struct BwdProblem {
+    const void *q, *k, *v, *o, *dO;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int B, Hq, Hkv, N, D;
+    float scale;
+    bool causal;
+    float *dq_acc;   // fp32 [B,Hq,N,D] inside the workspace
+    float *delta;    // fp32 [B,Hq,N]   inside the workspace
+};
+
+// Encodes a rank-3 bf16 tensor map over a [rows = N, cols = D] matrix per
+// head (dims {D, N, heads}) with a {64, box_rows, 1} box and 128-byte
+// swizzle.  Returns false if the driver rejects it.
+bool encode_bf16_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
+                      int box_rows);
+
+// Device status word of the current device (allocated statically).
+int *device_status_ptr();
+
+cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdProblem &pb, int *status, cudaStream_t stream);
+
+}  // namespace tattn
