@@ -37,6 +37,9 @@ constexpr int kBlockN = 128;   // keys per tile
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Lazy-rescale threshold in log2 units: the reference max is only raised when
+// a row's max grows by more than this (factor 2^8).
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct FwdCfg {
@@ -257,20 +260,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!ok) break;
             tc_fence_after();
             const uint32_t tS = tmem + lane_base + sbuf * kBlockN;
-            float t[kBlockN];
+            float x[kBlockN];
+            {
+                uint32_t rr[kBlockN];
+                tmem_ld128(tS, rr);
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tS + c * 32, rr);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) t[c * 32 + e] = __uint_as_float(rr[e]);
+                for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(rr[c]);
             }
             const int key0 = j * kBlockN;
             const bool diag = CAUSAL && (j == qt);
             const bool ragged = key0 + kBlockN > p.N;
+            // x holds raw q.k when `raw` (scale > 0, no bias): the max commutes
+            // with the positive scale and the scale folds into the exp2 FMA.
+            // Otherwise x is turned into log2-unit logits t here.
+            bool raw = !EXT && p.scale_log2 > 0.f;
 
             if constexpr (EXT) {
-                // Natural-unit logit x = scale*qk + bias; emitted before the mask.
+                // Natural-unit logit = scale*qk + bias; emitted before the mask.
                 const size_t roff = (static_cast<size_t>(bh) * p.N + q_row) * p.N + key0;
                 const float *brow = (p.bias && row_valid) ? p.bias + roff : nullptr;
                 float *erow = (p.emit && row_valid) ? p.emit + roff : nullptr;
@@ -279,16 +285,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     for (int c = 0; c < kBlockN; c += 4) {
                         float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
                         if (brow) bv = __ldg(reinterpret_cast<const float4 *>(brow + c));
-                        float4 x;
-                        x.x = fmaf(t[c + 0], p.scale, bv.x);
-                        x.y = fmaf(t[c + 1], p.scale, bv.y);
-                        x.z = fmaf(t[c + 2], p.scale, bv.z);
-                        x.w = fmaf(t[c + 3], p.scale, bv.w);
-                        if (erow) *reinterpret_cast<float4 *>(erow + c) = x;
-                        t[c + 0] = x.x * kLog2e;
-                        t[c + 1] = x.y * kLog2e;
-                        t[c + 2] = x.z * kLog2e;
-                        t[c + 3] = x.w * kLog2e;
+                        float4 y;
+                        y.x = fmaf(x[c + 0], p.scale, bv.x);
+                        y.y = fmaf(x[c + 1], p.scale, bv.y);
+                        y.z = fmaf(x[c + 2], p.scale, bv.z);
+                        y.w = fmaf(x[c + 3], p.scale, bv.w);
+                        if (erow) *reinterpret_cast<float4 *>(erow + c) = y;
+                        x[c + 0] = y.x * kLog2e;
+                        x[c + 1] = y.y * kLog2e;
+                        x[c + 2] = y.z * kLog2e;
+                        x[c + 3] = y.w * kLog2e;
                     }
                 } else {
                     const int lim = diag ? min(r + 1, kBlockN) : kBlockN;
@@ -297,43 +303,68 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         const bool inside = (c < lim) && (key0 + c < p.N);
                         float bval = 0.f;
                         if (brow && inside) bval = __ldg(brow + c);
-                        const float x = fmaf(t[c], p.scale, bval);
-                        if (erow && inside) erow[c] = x;
-                        t[c] = x * kLog2e;
+                        const float y = fmaf(x[c], p.scale, bval);
+                        if (erow && inside) erow[c] = y;
+                        x[c] = y * kLog2e;
                     }
                 }
             } else {
+                if (!raw) {
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) t[c] *= p.scale_log2;
+                    for (int c = 0; c < kBlockN; ++c) x[c] *= p.scale_log2;
+                }
             }
 
             if (diag || ragged) {
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c) {
                     const bool keep = (!diag || c <= r) && (key0 + c < p.N);
-                    t[c] = keep ? t[c] : -INFINITY;
+                    x[c] = keep ? x[c] : -INFINITY;
                 }
             }
-            float mt = t[0];
+            // Row max as a tree (8 independent chains of 3-input max).
+            float mx[8];
 #pragma unroll
-            for (int c = 1; c < kBlockN; ++c) mt = fmaxf(mt, t[c]);
-            const float m_new = fmaxf(m_run, mt);
+            for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < kBlockN; c += 16) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 8 + i]);
+            }
+            // (c runs 8, 24, ..., 120: elements 8..127 are all covered.)
+            const float mt_x = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                     fmaxf(mx[6], mx[7]));
+            const float m_tile = raw ? mt_x * p.scale_log2 : mt_x;
+            // Lazy rescale: keep the previous reference max while the new row
+            // max exceeds it by at most kRescaleLog2 (p stays <= 2^8); O/l and
+            // LSE are unchanged by the choice of reference.
+            float m_new = fmaxf(m_run, m_tile);
+            if (m_new - m_run <= kRescaleLog2) m_new = m_run;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = ex2(m_run - m_use);   // 0 on the first tile
 
-            float sum = 0.f;
+            const float cmul = raw ? p.scale_log2 : 1.f;
+            const uint64_t cm2 = f2pack(cmul, cmul);
+            const uint64_t nm2 = f2pack(-m_use, -m_use);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // (+0.0f, +0.0f) pairs
+            {
+                uint32_t pk[kBlockN / 2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = ex2(t[h * 64 + 2 * c] - m_use);
-                    const float p1 = ex2(t[h * 64 + 2 * c + 1] - m_use);
-                    sum += p0;
-                    sum += p1;
+                for (int c = 0; c < kBlockN / 2; ++c) {
+                    float t0, t1;
+                    f2unpack(ffma2(f2pack(x[2 * c], x[2 * c + 1]), cm2, nm2), t0, t1);
+                    const float p0 = ex2(t0), p1 = ex2(t1);
+                    acc[c & 3] = fadd2(acc[c & 3], f2pack(p0, p1));
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(tS + h * 32, pk);
+                tmem_st64(tS, pk);
+            }
+            float sum;
+            {
+                const uint64_t a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+                float u0, u1;
+                f2unpack(fadd2(a01, a23), u0, u1);
+                sum = u0 + u1;
             }
             l_run = fmaf(l_run, alpha, sum);
 
@@ -344,14 +375,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tO = tmem + lane_base + C::kColO;
+                const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tO + c * 32, rr);
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t rr[64];
+                    tmem_ld64(tO + c * 64, rr);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                    tmem_st32(tO + c * 32, rr);
+                    for (int e = 0; e < 64; e += 2) {
+                        float o0 = __uint_as_float(rr[e]), o1 = __uint_as_float(rr[e + 1]);
+                        f2unpack(fmul2(f2pack(o0, o1), a2), o0, o1);
+                        rr[e] = __float_as_uint(o0);
+                        rr[e + 1] = __float_as_uint(o1);
+                    }
+                    tmem_st64(tO + c * 64, rr);
                 }
             }
             tmem_st_wait();
@@ -367,22 +403,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const float inv_l = 1.f / l_run;
             const uint32_t tO = tmem + lane_base + C::kColO;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tO + c * 32, rr);
-                uint32_t w[16];
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t rr[64];
+                tmem_ld64(tO + c * 64, rr);
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * inv_l,
-                                       __uint_as_float(rr[2 * e + 1]) * inv_l);
+                for (int pc = 0; pc < 8; ++pc) {       // 16-byte pieces of this 64-column atom
+                    uint32_t w[4];
 #pragma unroll
-                for (int pc = 0; pc < 4; ++pc) {
-                    const int d0 = c * 32 + pc * 8;        // first column of this 16-byte piece
-                    const int atom = d0 >> 6;
-                    const int piece = (d0 & 63) >> 3;
-                    const uint32_t addr = sb + C::kOffQ + atom * C::kChunkBytes + r * 128 +
-                                          (static_cast<uint32_t>(piece ^ (r & 7)) << 4);
-                    st_shared_v4(addr, w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(rr[pc * 8 + 2 * e]) * inv_l,
+                                           __uint_as_float(rr[pc * 8 + 2 * e + 1]) * inv_l);
+                    const uint32_t addr = sb + C::kOffQ + c * C::kChunkBytes + r * 128 +
+                                          (static_cast<uint32_t>(pc ^ (r & 7)) << 4);
+                    st_shared_v4(addr, w[0], w[1], w[2], w[3]);
                 }
             }
             if (p.lse && row_valid)
