@@ -106,9 +106,11 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, const float *b
                      float *emit_logits, void *stream);
 
 /*
- * Bytes of device workspace attn_bwd needs for this shape (fp32 dQ
- * accumulator [B,Hq,N,D] and fp32 Delta [B,Hq,N], each rounded up to 256
- * bytes).  Returns 0 for an empty problem or invalid sizes.
+ * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
+ * accumulator [B,Hq,N,D], plus two fp32 per-row arrays [B*Hq, NP]
+ * (NP = N rounded up to a multiple of 128) holding LSE*log2(e) and
+ * Delta_i = sum_d dO_id O_id; each region rounded up to 256 bytes.
+ * Returns 0 for an empty problem or invalid sizes.
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D);
 

@@ -88,9 +88,12 @@ def test_bwd_rejects_bad_arguments(ta, kw, code):
 
 
 def test_workspace_size(ta):
-    # fp32 dQ accumulator + fp32 Delta, each rounded up to 256 bytes
-    assert ta.attn_bwd_workspace_size(1, 16, 16, 16384, 128) == 16 * 16384 * 128 * 4 + 16 * 16384 * 4
-    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 64) == 768 + 256
-    assert ta.attn_bwd_workspace_size(1, 1, 1, 5, 64) == 1280 + 256
+    # fp32 dQ accumulator + two fp32 per-row arrays padded to 128-row tiles,
+    # each region rounded up to 256 bytes
+    assert ta.attn_bwd_workspace_size(1, 16, 16, 16384, 128) == (16 * 16384 * 128 * 4
+                                                                 + 2 * 16 * 16384 * 4)
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 64) == 768 + 2 * 512
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 5, 64) == 1280 + 2 * 512
+    assert ta.attn_bwd_workspace_size(2, 3, 1, 130, 64) == (6 * 130 * 64 * 4 + 2 * 6 * 256 * 4)
     assert ta.attn_bwd_workspace_size(0, 1, 1, 3, 64) == 0
     assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 96) == 0

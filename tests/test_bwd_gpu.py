@@ -1,0 +1,103 @@
+"""GPU parity of the recompute backward (C ABI) against the fp64 oracle's
+exact gradient: every element on small shapes (several tiles, ragged tails,
+grouped heads), and 256 query rows (dQ) plus 256 key rows (dK, dV) at the
+full long-sequence size."""
+import math
+
+import numpy as np
+import pytest
+
+from helpers import check_grad, make_qkv, sample_rows, to_oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ta():
+    import tiled_attention_02_gb300 as ta
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ta.build()
+    return ta
+
+
+def gpu_fwd_bwd(ta, x, causal):
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ta.attn_fwd(q, k, v, causal=causal)
+    dq, dk, dv = ta.attn_bwd(q, k, v, o, lse, do, causal=causal)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    return dq, dk, dv
+
+
+SHAPES = [
+    # B, Hq, Hkv, N, D
+    (1, 2, 2, 256, 128),
+    (1, 4, 2, 384, 64),      # grouped heads: dK, dV summed over the group
+    (1, 3, 1, 200, 128),     # ragged tail
+    (2, 2, 2, 129, 64),      # one row past a tile
+    (1, 1, 1, 1, 128),       # single row
+    (1, 6, 2, 256, 128),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}H{s[1]}kv{s[2]}N{s[3]}D{s[4]}" for s in SHAPES])
+def test_bwd_parity_small(ta, orc, shape, causal):
+    B, Hq, Hkv, N, D = shape
+    x = make_qkv(B, Hq, Hkv, N, D, seed=N + D + 1, with_do=True)
+    dq, dk, dv = gpu_fwd_bwd(ta, x, causal)
+    ref = orc.backward(*(to_oracle(x[n]) for n in ("q", "k", "v", "do")),
+                       scale=1 / math.sqrt(D), causal=causal)
+    check_grad(dq, ref["dq"], f"dq {shape}")
+    check_grad(dk, ref["dk"], f"dk {shape}")
+    check_grad(dv, ref["dv"], f"dv {shape}")
+
+
+def test_bwd_every_output_written(ta):
+    x = make_qkv(1, 2, 1, 333, 128, seed=2, with_do=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ta.attn_fwd(q, k, v, causal=True)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    ta.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+
+
+def test_bwd_workspace_contents_do_not_matter(ta):
+    """The workspace is fully initialised by the call itself."""
+    x = make_qkv(1, 2, 2, 256, 64, seed=3, with_do=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ta.attn_fwd(q, k, v, causal=True)
+    need = ta.attn_bwd_workspace_size(1, 2, 2, 256, 64)
+    ws1 = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ws2 = torch.full((need,), 0x7F, dtype=torch.uint8, device="cuda")
+    a = ta.attn_bwd(q, k, v, o, lse, do, causal=True, workspace=ws1)
+    b = ta.attn_bwd(q, k, v, o, lse, do, causal=True, workspace=ws2)
+    torch.cuda.synchronize()
+    for u, w in zip(a, b):
+        assert (u.float() - w.float()).abs().max().item() < 1e-2
+
+
+def test_bwd_full_size_sampled(ta, orc):
+    """B=1, H=16, N=16384, D=128, causal: 256 sampled query rows (dQ) and
+    256 sampled key rows (dK, dV) against the oracle's exact gradient."""
+    B, H, N, D = 1, 16, 16384, 128
+    x = make_qkv(B, H, H, N, D, seed=0, with_do=True)
+    dq, dk, dv = gpu_fwd_bwd(ta, x, True)
+    q_rows = sample_rows(B, H, N, 256, seed=3)
+    rng = np.random.default_rng(4)
+    heads = rng.choice(H, size=4, replace=False)
+    k_rows = np.unique(np.concatenate([
+        np.array([h * N, h * N + N - 1, h * N + 127, h * N + 128]) for h in heads] + [
+        heads[rng.integers(0, 4, 240)] * N + rng.integers(0, N, 240)]))
+    ref = orc.backward_sampled(*(to_oracle(x[n]) for n in ("q", "k", "v", "do")),
+                               scale=1 / math.sqrt(D), causal=True, q_rows=q_rows, k_rows=k_rows)
+    qr, kr = torch.from_numpy(q_rows).cuda(), torch.from_numpy(k_rows).cuda()
+    check_grad(dq.reshape(-1, D)[qr], ref["dq"], "dq sampled")
+    check_grad(dk.reshape(-1, D)[kr], ref["dk"], "dk sampled")
+    check_grad(dv.reshape(-1, D)[kr], ref["dv"], "dv sampled")

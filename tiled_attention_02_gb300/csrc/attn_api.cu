@@ -73,6 +73,18 @@ bool encode_bf16_rows(CUtensorMap *map, const void *base, int D, int N, long lon
     return r == CUDA_SUCCESS;
 }
 
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int D) {
+    auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    const size_t prow = static_cast<size_t>(B) * Hq * (((static_cast<size_t>(N) + 127) / 128) * 128);
+    BwdWorkspace w;
+    w.dq_acc = 0;
+    w.lse2 = round256(rows * D * sizeof(float));
+    w.delta = w.lse2 + round256(prow * sizeof(float));
+    w.total = w.delta + round256(prow * sizeof(float));
+    return w;
+}
+
 int *device_status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -129,12 +141,11 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, const float *b
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D) {
     bool empty = false;
     if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
-    auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t rows = static_cast<size_t>(B) * Hq * N;
-    return round256(rows * D * sizeof(float)) + round256(rows * sizeof(float));
+    return bwd_workspace_layout(B, Hq, N, D).total;
 }
 
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -150,10 +161,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
     for (const void *p : bf)
         if (!aligned(p, 16)) return ATTN_ERR_INVALID;
     if (!aligned(lse, 4) || !aligned(workspace, 256)) return ATTN_ERR_INVALID;
-    const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, N, D);
-    if (workspace_bytes < need) return ATTN_ERR_INVALID;
-    const size_t rows = static_cast<size_t>(B) * Hq * N;
-    const size_t acc_bytes = (rows * D * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    const BwdWorkspace wl = bwd_workspace_layout(B, Hq, N, D);
+    if (workspace_bytes < wl.total) return ATTN_ERR_INVALID;
     BwdProblem pb;
     pb.q = q;
     pb.k = k;
@@ -171,8 +180,11 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
     pb.D = D;
     pb.scale = scale;
     pb.causal = causal != 0;
-    pb.dq_acc = static_cast<float *>(workspace);
-    pb.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc_bytes);
+    char *ws = static_cast<char *>(workspace);
+    pb.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
+    pb.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
+    pb.delta = reinterpret_cast<float *>(ws + wl.delta);
+    pb.NP = ((N + 127) / 128) * 128;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
     cudaError_t e = launch_bwd(pb, status, static_cast<cudaStream_t>(stream));

@@ -1,9 +1,522 @@
-// attn_bwd.cu -- recompute-based attention backward (placeholder until the
-// tcgen05 backward kernels land).
+// attn_bwd.cu -- recompute-based attention backward for GB300 (sm_103a).
+//
+// The backward of exact attention from the saved per-row log-sum-exp only
+// (kwkr.cn/news/592482, section 2.4; "FlashAttention原理与Triton实战",
+// sections 2.3 and 4.3): P is recomputed tile by tile, the chain rule gives
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - Delta),  Delta_i = dO_i . O_i,
+//   dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three launches on the caller's stream:
+//  1. bwd_pre_kernel    Delta_i (fp32, from the bf16 O and dO), LSE * log2(e)
+//                       padded to whole 128-row tiles, and a zeroed fp32 dQ
+//                       accumulator -- all in the caller's workspace.
+//  2. bwd_main_kernel   one CTA per (batch, kv head, 128-key tile); loops over
+//                       every 128-row query tile of every query head of the
+//                       group that can see those keys.  Per query tile:
+//                         S^T  = K Q^T       tcgen05.mma -> TMEM
+//                         dP^T = V dO^T      tcgen05.mma -> TMEM
+//                         P^T  = 2^(S^T scale log2e - LSE log2e)   (bf16 -> TMEM)
+//                         dS^T = P^T o (dP^T - Delta) * scale     (bf16 -> smem)
+//                         dV  += P^T dO      tcgen05.mma, A from TMEM
+//                         dK  += dS^T Q      tcgen05.mma
+//                         dQ   = dS K        tcgen05.mma -> TMEM, then added
+//                                            into the fp32 accumulator with
+//                                            vector reductions
+//                       dK, dV stay in TMEM for the whole loop (summed over the
+//                       query heads of a kv group) and are stored once.
+//  3. bwd_dq_kernel     fp32 dQ accumulator -> bf16 dQ.
+//
+// Warp roles of the main kernel (320 threads, one CTA per SM):
+//   warps 0-3  thread r owns key row r: P^T, dS^T; epilogue of dK, dV.
+//   warps 4-7  thread r owns query row r of the dQ tile: TMEM -> red.global.
+//   warp 8     TMA producer (K, V once; Q, dO, LSE, Delta per query tile).
+//   warp 9     TMEM allocator and tcgen05.mma issuer.
+// TMEM columns: S^T/P^T 0..127, dP^T/dQ 128..255, dV 256.., dK 256+D...
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <algorithm>
 
 namespace tattn {
+namespace {
 
-cudaError_t launch_bwd(const BwdProblem &, int *, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kTile = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// --------------------------------------------------------------- preprocess
+
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dO,
+               const float *__restrict__ lse, float *__restrict__ lse2,
+               float *__restrict__ delta, float *__restrict__ dq_acc, int N, int NP) {
+    constexpr int kLanesPerRow = D / 8;          // 8 bf16 (16 bytes) per lane
+    constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int row0 = blockIdx.y * kTile;
+    const int sub = lane % kLanesPerRow;
+    for (int rr = warp * kRowsPerWarp + lane / kLanesPerRow; rr < kTile; rr += 8 * kRowsPerWarp) {
+        const int row = row0 + rr;
+        const bool valid = row < N;
+        float acc = 0.f;
+        const size_t off = (static_cast<size_t>(bh) * N + row) * D + sub * 8;
+        if (valid) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(o + off);
+            const uint4 b = *reinterpret_cast<const uint4 *>(dO + off);
+            const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+            const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = __bfloat1622float2(pa[e]);
+                const float2 fb = __bfloat1622float2(pb[e]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+            float4 *z = reinterpret_cast<float4 *>(dq_acc + off);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (sub == 0) {
+            const size_t prow = static_cast<size_t>(bh) * NP + row;
+            lse2[prow] = valid ? lse[static_cast<size_t>(bh) * N + row] * kLog2e : INFINITY;
+            delta[prow] = valid ? acc : 0.f;
+        }
+    }
+}
+
+// ------------------------------------------------------------ dQ convert
+
+__global__ void __launch_bounds__(256)
+bwd_dq_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, size_t n8) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+        uint4 w;
+        w.x = pack_bf16x2(a.x, a.y);
+        w.y = pack_bf16x2(a.z, a.w);
+        w.z = pack_bf16x2(b.x, b.y);
+        w.w = pack_bf16x2(b.z, b.w);
+        reinterpret_cast<uint4 *>(dq)[i] = w;
+    }
+}
+
+// ------------------------------------------------------------ main kernel
+
+constexpr int kThreads = 320;
+constexpr int kMaxSmem = 232448;   // opt-in shared memory per block on sm_100/sm_103
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = kTile * 128;
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kTileBytes;
+    static constexpr int kOffStage = 2 * kTileBytes;          // 2 stages of {Q, dO}
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kOffRows = kOffStage + 2 * kStageBytes;   // lse2[2][128], delta[2][128]
+    static constexpr int kOffDS = ((kOffRows + 4 * kTile * 4) + 1023) & ~1023;
+    static constexpr int kDSBytes = kTile * kTile * 2;
+    static constexpr int kOffBar = kOffDS + kDSBytes;
+    static constexpr int kBarKV = 0;
+    static constexpr int kBarQDFull = 1;     // 2
+    static constexpr int kBarQDEmpty = 3;    // 2
+    static constexpr int kBarSFull = 5;
+    static constexpr int kBarPReady = 6;
+    static constexpr int kBarDQFull = 7;
+    static constexpr int kBarDQEmpty = 8;
+    static constexpr int kBarDSFree = 9;
+    static constexpr int kBarAccDone = 10;
+    static constexpr int kBarDrain = 11;
+    static constexpr int kNumBars = 12;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kUsed = kOffMisc + 16;
+    static constexpr int kSmemBytes = (kUsed + 1023 <= kMaxSmem) ? kUsed + 1023 : kMaxSmem;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static_assert(kUsed <= kMaxSmem, "shared memory budget");
+};
+
+struct BwdParams {
+    const float *lse2;
+    const float *delta;
+    float *dq_acc;
+    int *status;
+    int N, NP, Hq, Hkv, group, BHkv, n_tiles;
+    float scale, scale_log2;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > 20ull * 1000ull * 1000ull) break;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Writes 64 packed-bf16 words (128 columns) of row r into a 128-row tile
+// staged in the 128-byte swizzled layout TMA and tcgen05 use.
+__device__ __forceinline__ void stage_row64(uint32_t tile, int r, int atom, const uint32_t *w) {
+#pragma unroll
+    for (int pc = 0; pc < 8; ++pc) {
+        const uint32_t addr = tile + atom * (kTile * 128) + r * 128 +
+                              (static_cast<uint32_t>(pc ^ (r & 7)) << 4);
+        st_shared_v4(addr, w[4 * pc], w[4 * pc + 1], w[4 * pc + 2], w[4 * pc + 3]);
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // The layout needs a 1024-byte aligned base; refuse to run if the
+    // allocation cannot hold it after alignment.
+    if (smem - smem_raw + C::kUsed > C::kSmemBytes) {
+        if (threadIdx.x == 0) atomicCAS(p.status, kStatusOk, kStatusDeviceCheck);
+        return;
+    }
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Heaviest key tiles first under the causal mask (tile 0 sees every query tile).
+    const int kt = blockIdx.x / p.BHkv;
+    const int bh_kv = blockIdx.x % p.BHkv;
+    const int b = bh_kv / p.Hkv, g = bh_kv % p.Hkv;
+    const int q_lo = CAUSAL ? kt : 0;
+    const int nq = p.n_tiles - q_lo;              // query tiles per query head
+    const int n_items = p.group * nq;
+
+    auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    const AbortCtl ac{abort_flag, p.status};
+    auto item_qi = [&](int j) { return q_lo + j % nq; };
+    auto item_bhq = [&](int j) { return b * p.Hq + g * p.group + j / nq; };
+    const uint32_t s_rows = sb + C::kOffRows;   // lse2[s][128] then delta[s][128]
+    const float *rows_f = reinterpret_cast<const float *>(smem + C::kOffRows);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(bar(C::kBarKV), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(C::kBarQDFull + s), 1);
+            mbar_init(bar(C::kBarQDEmpty + s), 1);
+        }
+        mbar_init(bar(C::kBarSFull), 1);
+        mbar_init(bar(C::kBarPReady), kTile);
+        mbar_init(bar(C::kBarDQFull), 1);
+        mbar_init(bar(C::kBarDQEmpty), kTile);
+        mbar_init(bar(C::kBarDSFree), 1);
+        mbar_init(bar(C::kBarAccDone), 1);
+        mbar_init(bar(C::kBarDrain), 1);
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(sb + C::kOffK + c * C::kChunkBytes, &tmK, bar(C::kBarKV), c * 64,
+                            kt * kTile, bh_kv);
+                tma_load_3d(sb + C::kOffV + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64,
+                            kt * kTile, bh_kv);
+            }
+            int issued = 0;
+            for (int j = 0; j < n_items; ++j) {
+                const int s = j & 1;
+                if (j >= 2) ok = mbar_wait(bar(C::kBarQDEmpty + s), ((j >> 1) - 1) & 1, ac);
+                if (!ok) break;
+                const int qi = item_qi(j), bhq = item_bhq(j);
+                const uint32_t fb = bar(C::kBarQDFull + s);
+                mbar_arrive_expect_tx(fb, 2 * C::kTileBytes + 2 * kTile * 4);
+                const uint32_t st = sb + C::kOffStage + s * C::kStageBytes;
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(st + c * C::kChunkBytes, &tmQ, fb, c * 64, qi * kTile, bhq);
+                    tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tmdO, fb, c * 64,
+                                qi * kTile, bhq);
+                }
+                const size_t prow = static_cast<size_t>(bhq) * p.NP + qi * kTile;
+                bulk_load(s_rows + s * kTile * 4, p.lse2 + prow, kTile * 4, fb);
+                bulk_load(s_rows + (2 + s) * kTile * 4, p.delta + prow, kTile * 4, fb);
+                issued = j + 1;
+            }
+            if (!ok) {
+                drain_wait(bar(C::kBarKV), 0);
+                for (int j = max(issued - 2, 0); j < issued; ++j)
+                    drain_wait(bar(C::kBarQDFull + (j & 1)), (j >> 1) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, false, false);
+            constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, false, true);   // dV, dK
+            constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, D, true, true);     // dQ
+            bool ok = mbar_wait(bar(C::kBarKV), 0, ac);
+            for (int j = 0; j < n_items && ok; ++j) {
+                const int s = j & 1;
+                ok = mbar_wait(bar(C::kBarQDFull + s), (j >> 1) & 1, ac);
+                if (ok && j > 0) ok = mbar_wait(bar(C::kBarDQEmpty), (j - 1) & 1, ac);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sQ = sb + C::kOffStage + s * C::kStageBytes;
+                const uint32_t sdO = sQ + C::kTileBytes;
+                const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV, sDS = sb + C::kOffDS;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024),
+                           sdesc_sw128(sQ + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {   // dP^T = V dO^T
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024),
+                           sdesc_sw128(sdO + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(C::kBarSFull));
+                ok = mbar_wait(bar(C::kBarPReady), j & 1, ac);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {   // dV += P^T dO  (A in TMEM)
+                    mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                           sdesc_sw128(sdO + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {   // dK += dS^T Q
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + off, 16, 1024),
+                           sdesc_sw128(sQ + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(C::kBarQDEmpty + s));
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {   // dQ = dS K (both MN-major)
+                    mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + kk * 2048, C::kChunkBytes, 1024),
+                           sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), kIdDQ,
+                           kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(C::kBarDQFull));
+                mma_commit(bar(C::kBarDSFree));
+            }
+            if (ok) {
+                mma_commit(bar(C::kBarAccDone));
+            } else {
+                mma_commit(bar(C::kBarDrain));
+                drain_wait(bar(C::kBarDrain), 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------ dQ drain warpgroup
+        const int qr = threadIdx.x - 128;
+        const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16) + C::kColDP;
+        for (int j = 0; j < n_items; ++j) {
+            if (!mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac)) break;
+            tc_fence_after();
+            const int row = item_qi(j) * kTile + qr;
+            const bool valid = row < p.N;
+            float *dst = p.dq_acc + (static_cast<size_t>(item_bhq(j)) * p.N + row) * D;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t rr[64];
+                tmem_ld64(tDQ + c * 64, rr);
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 64; e += 4)
+                        red_add_v4(dst + c * 64 + e, __uint_as_float(rr[e]),
+                                   __uint_as_float(rr[e + 1]), __uint_as_float(rr[e + 2]),
+                                   __uint_as_float(rr[e + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarDQEmpty));
+        }
+    } else {
+        // ----------------------------------------------- P / dS warpgroup
+        const int kr = threadIdx.x;   // key row within the tile == TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::kColS;
+        const uint32_t tDP = tmem + lane_base + C::kColDP;
+        const uint32_t sDS = sb + C::kOffDS;
+        bool ok = true;
+        for (int j = 0; j < n_items; ++j) {
+            const int s = j & 1;
+            ok = mbar_wait_warp(bar(C::kBarSFull), j & 1, ac);
+            if (ok) ok = mbar_wait_warp(bar(C::kBarQDFull + s), (j >> 1) & 1, ac);
+            if (ok && j > 0) ok = mbar_wait_warp(bar(C::kBarDSFree), (j - 1) & 1, ac);
+            if (!ok) break;
+            tc_fence_after();
+            const bool diag = CAUSAL && (item_qi(j) == kt);
+            const float *lse2 = rows_f + s * kTile;
+            const float *dlt = rows_f + (2 + s) * kTile;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sr[64], dr[64];
+                tmem_ld64(tS + h * 64, sr);
+                tmem_ld64(tDP + h * 64, dr);
+                uint32_t pw[32], dw[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const int q = h * 64 + c;
+                    float p0 = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -lse2[q]));
+                    float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -lse2[q + 1]));
+                    if (diag) {
+                        p0 = (kr <= q) ? p0 : 0.f;
+                        p1 = (kr <= q + 1) ? p1 : 0.f;
+                    }
+                    const float d0 = p0 * (__uint_as_float(dr[c]) - dlt[q]) * p.scale;
+                    const float d1 = p1 * (__uint_as_float(dr[c + 1]) - dlt[q + 1]) * p.scale;
+                    pw[c >> 1] = pack_bf16x2(p0, p1);
+                    dw[c >> 1] = pack_bf16x2(d0, d1);
+                }
+                tmem_st32(tS + h * 32, pw);   // P^T bf16 pairs over columns already read
+                stage_row64(sDS, kr, h, dw);
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarPReady));
+        }
+
+        // ------------------------------------------------ epilogue: dK, dV
+        if (ok) ok = mbar_wait_warp(bar(C::kBarAccDone), 0, ac);
+        const uint32_t stV = sb + C::kOffStage;                  // stage 0 Q buffer
+        const uint32_t stK = sb + C::kOffStage + C::kTileBytes;  // stage 0 dO buffer
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+                const uint32_t dst = which == 0 ? stV : stK;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t rr[64];
+                    tmem_ld64(tmem + lane_base + col + c * 64, rr);
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                    stage_row64(dst, kr, c, w);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        named_bar_sync(1, kTile);
+        if (threadIdx.x == 0 && *abort_flag == 0) {
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_store_3d(&tmdV, stV + c * C::kChunkBytes, c * 64, kt * kTile, bh_kv);
+                tma_store_3d(&tmdK, stK + c * C::kChunkBytes, c * 64, kt * kTile, bh_kv);
+            }
+            tma_store_commit();
+            tma_store_wait_read();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    const long long BH = static_cast<long long>(pb.B) * pb.Hq;
+    const long long BHkv = static_cast<long long>(pb.B) * pb.Hkv;
+    const int n_tiles = pb.NP / kTile;
+
+    // 1. Delta, LSE*log2(e), zeroed dQ accumulator.
+    bwd_pre_kernel<D><<<dim3(static_cast<unsigned>(BH), n_tiles), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(pb.o), static_cast<const __nv_bfloat16 *>(pb.dO),
+        pb.lse, pb.lse2, pb.delta, pb.dq_acc, pb.N, pb.NP);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // 2. main kernel.
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (!encode_bf16_rows(&tq, pb.q, D, pb.N, BH, kTile) ||
+        !encode_bf16_rows(&tk, pb.k, D, pb.N, BHkv, kTile) ||
+        !encode_bf16_rows(&tv, pb.v, D, pb.N, BHkv, kTile) ||
+        !encode_bf16_rows(&tdo, pb.dO, D, pb.N, BH, kTile) ||
+        !encode_bf16_rows(&tdk, pb.dk, D, pb.N, BHkv, kTile) ||
+        !encode_bf16_rows(&tdv, pb.dv, D, pb.N, BHkv, kTile))
+        return cudaErrorInvalidValue;
+    BwdParams prm;
+    prm.lse2 = pb.lse2;
+    prm.delta = pb.delta;
+    prm.dq_acc = pb.dq_acc;
+    prm.status = status;
+    prm.N = pb.N;
+    prm.NP = pb.NP;
+    prm.Hq = pb.Hq;
+    prm.Hkv = pb.Hkv;
+    prm.group = pb.Hq / pb.Hkv;
+    prm.BHkv = static_cast<int>(BHkv);
+    prm.n_tiles = n_tiles;
+    prm.scale = pb.scale;
+    prm.scale_log2 = pb.scale * kLog2e;
+    const unsigned grid = static_cast<unsigned>(n_tiles * BHkv);
+    auto kern = pb.causal ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // 3. fp32 dQ accumulator -> bf16 dQ.
+    const size_t n8 = static_cast<size_t>(BH) * pb.N * D / 8;
+    const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
+    bwd_dq_kernel<<<blocks, 256, 0, stream>>>(pb.dq_acc, static_cast<__nv_bfloat16 *>(pb.dq), n8);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdProblem &pb, int *status, cudaStream_t stream) {
+    if (pb.D == 64) return launch_d<64>(pb, status, stream);
+    return launch_d<128>(pb, status, stream);
+}
 
 }  // namespace tattn

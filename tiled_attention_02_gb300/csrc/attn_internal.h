@@ -30,8 +30,17 @@ struct BwdProblem {
     float scale;
     bool causal;
     float *dq_acc;   // fp32 [B,Hq,N,D] inside the workspace
-    float *delta;    // fp32 [B,Hq,N]   inside the workspace
+    float *lse2;     // fp32 [B*Hq, NP]: LSE * log2(e), +inf on padding rows
+    float *delta;    // fp32 [B*Hq, NP]: rowsum(dO * O), 0 on padding rows
+    int NP;          // N rounded up to the 128-row tile
 };
+
+// Byte offsets of the three workspace regions (each 256-byte aligned) and
+// the total size, for a validated shape.
+struct BwdWorkspace {
+    size_t dq_acc, lse2, delta, total;
+};
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int D);
 
 // Encodes a rank-3 bf16 tensor map over a [rows = N, cols = D] matrix per
 // head (dims {D, N, heads}) with a {64, box_rows, 1} box and 128-byte
