@@ -139,6 +139,49 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      int B, int Hq, int Hkv, int N, int D, float scale, int causal,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Size of the fixed device scratch behind attn_bwd_noalloc: 32 MiB.  A shape
+ * fits when attn_bwd_workspace_size(B, Hq, Hkv, N, D) is at most this many
+ * bytes -- about 64 thousand query rows (B*Hq*N) at D = 128, about 127
+ * thousand at D = 64.
+ */
+#define ATTN_BWD_NOALLOC_SCRATCH_BYTES 33554432
+
+/*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point; it is
+ * an addition of this library.
+ *
+ * Who needs it: a caller that cannot call cudaMalloc -- a host engine that
+ * owns every device allocation and hands the libraries it loads no
+ * allocator, or code that must not trigger the device-wide synchronisation
+ * cudaMalloc and cudaFree can cause -- has no way to provide attn_bwd's
+ * workspace.  This call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  Its scratch is one fixed array of
+ * ATTN_BWD_NOALLOC_SCRATCH_BYTES in device memory, reserved on every device
+ * that loads the library and held until the process exits.
+ *
+ * Arguments, layouts, results and error codes are those of attn_bwd, minus
+ * the workspace.  In addition:
+ *  - a shape whose workspace would exceed ATTN_BWD_NOALLOC_SCRATCH_BYTES is
+ *    rejected with ATTN_ERR_UNSUPPORTED before anything is launched (use
+ *    attn_bwd with your own workspace for it);
+ *  - the first call on a device looks up that device's address of the
+ *    scratch array (cudaGetSymbolAddress, with the device current) and
+ *    caches it; make that first call before any stream capture;
+ *  - every call shares the one array and the array keeps whatever the last
+ *    call left in it; each call first rewrites everything it later reads, so
+ *    leftover contents never change a result;
+ *  - calls whose kernels overlap on the GPU (different streams, or several
+ *    host threads) race on the shared scratch and give wrong results:
+ *    order them, e.g. issue them on one stream.
+ */
+attn_status attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dO,
+                             void *dq, void *dk, void *dv,
+                             int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                             void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *attn_status_string(attn_status status);
 

@@ -32,8 +32,11 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_DEVICE_CHECK = 5
 
 # Every symbol include/tattn.h declares.
-EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
-            "attn_last_device_status", "attn_version")
+EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_noalloc",
+            "attn_status_string", "attn_last_device_status", "attn_version")
+
+# Size of the fixed device scratch attn_bwd_noalloc uses (include/tattn.h).
+ATTN_BWD_NOALLOC_SCRATCH_BYTES = 33554432
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +71,9 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
                                    sz, vp]
             L.attn_bwd.restype = i
+            L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                           f, i, vp]
+            L.attn_bwd_noalloc.restype = i
             L.attn_status_string.argtypes = [i]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_last_device_status.argtypes = [vp]
@@ -183,6 +189,41 @@ def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = 
                       workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def raw_attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal,
+                         stream) -> int:
+    return lib().attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D,
+                                  ctypes.c_float(scale), int(causal), stream)
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = False,
+                     dq=None, dk=None, dv=None, stream=None):
+    """Backward through the allocation-free C entry point: the library's own
+    fixed device scratch replaces the workspace (for callers that cannot
+    allocate device memory).  Output tensors are allocated here only when
+    not given.  Returns (dq, dk, dv)."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    for t, name, dt, shp in ((q, "q", torch.bfloat16, (B, Hq, N, D)),
+                             (k, "k", torch.bfloat16, (B, Hkv, N, D)),
+                             (v, "v", torch.bfloat16, (B, Hkv, N, D)),
+                             (o, "o", torch.bfloat16, (B, Hq, N, D)),
+                             (lse, "lse", torch.float32, (B, Hq, N)),
+                             (do, "do", torch.bfloat16, (B, Hq, N, D))):
+        _check(t, name, dt, shp)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = raw_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, Hq, Hkv, N, D, scale, causal,
+                              _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_noalloc")
     return dq, dk, dv
 
 
