@@ -57,20 +57,35 @@ attn_status check_sizes(int B, int Hq, int Hkv, int N, int D, float scale, bool 
 
 }  // namespace
 
-bool encode_bf16_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
-                      int box_rows) {
+namespace {
+// Rank-3 tiled map over [heads, N, D] (dims {D, N, heads}), 128-byte rows in
+// the box ({128 / elem_bytes, box_rows, 1}), 128-byte swizzle.
+bool encode_rows(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base,
+                 int D, int N, long long heads, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(heads)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                             static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(N)};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem_bytes,
+                             static_cast<cuuint64_t>(D) * elem_bytes * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes),
+                         static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool encode_bf16_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
+                      int box_rows) {
+    return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, N, heads, box_rows);
+}
+
+bool encode_f32_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
+                     int box_rows) {
+    return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, N, heads, box_rows);
 }
 
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int D) {

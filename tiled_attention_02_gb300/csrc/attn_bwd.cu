@@ -19,16 +19,17 @@
 //                         dS^T = P^T o (dP^T - Delta) * scale     (bf16 -> smem)
 //                         dV  += P^T dO      tcgen05.mma, A from TMEM
 //                         dK  += dS^T Q      tcgen05.mma
-//                         dQ   = dS K        tcgen05.mma -> TMEM, then added
-//                                            into the fp32 accumulator with
-//                                            vector reductions
+//                         dQ   = dS K        tcgen05.mma -> TMEM, staged to
+//                                            smem and added into the fp32
+//                                            accumulator by TMA bulk
+//                                            reductions
 //                       dK, dV stay in TMEM for the whole loop (summed over the
 //                       query heads of a kv group) and are stored once.
 //  3. bwd_dq_kernel     fp32 dQ accumulator -> bf16 dQ.
 //
 // Warp roles of the main kernel (320 threads, one CTA per SM):
 //   warps 0-3  thread r owns key row r: P^T, dS^T; epilogue of dK, dV.
-//   warps 4-7  thread r owns query row r of the dQ tile: TMEM -> red.global.
+//   warps 4-7  thread r owns query row r of the dQ tile: TMEM -> smem -> TMA add.
 //   warp 8     TMA producer (K, V once; Q, dO, LSE, Delta per query tile).
 //   warp 9     TMEM allocator and tcgen05.mma issuer.
 // TMEM columns: S^T/P^T 0..127, dP^T/dQ 128..255, dV 256.., dK 256+D...
@@ -166,11 +167,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
-}
 
 // Writes 64 packed-bf16 words (128 columns) of row r into a 128-row tile
 // staged in the 128-byte swizzled layout TMA and tcgen05 use.
@@ -188,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -218,7 +214,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto item_qi = [&](int j) { return q_lo + j % nq; };
     auto item_bhq = [&](int j) { return b * p.Hq + g * p.group + j / nq; };
     const uint32_t s_rows = sb + C::kOffRows;   // lse2[s][128] then delta[s][128]
-    const float *rows_f = reinterpret_cast<const float *>(smem + C::kOffRows);
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -327,7 +322,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                            sdesc_sw128(sQ + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(C::kBarQDEmpty + s));
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {   // dQ = dS K (both MN-major)
                     mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + kk * 2048, C::kChunkBytes, 1024),
@@ -347,29 +341,50 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------ dQ drain warpgroup
+        // dQ(j) is staged (fp32, 128-byte swizzled boxes of 32 columns) in the
+        // Q/dO buffers of item j's stage -- exactly 128 x D x 4 bytes, free
+        // once item j's MMAs are done -- and added into the fp32 accumulator
+        // with TMA bulk reductions.  The stage is handed back to the producer
+        // only after the reductions have read it.
         const int qr = threadIdx.x - 128;
         const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16) + C::kColDP;
         for (int j = 0; j < n_items; ++j) {
-            if (!mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac)) break;
+            const int s = j & 1;
+            const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
+            // All four drain warps leave together (they meet at a barrier below).
+            if (named_bar_or(2, kTile, !got)) break;
             tc_fence_after();
-            const int row = item_qi(j) * kTile + qr;
-            const bool valid = row < p.N;
-            float *dst = p.dq_acc + (static_cast<size_t>(item_bhq(j)) * p.N + row) * D;
+            const uint32_t stage = sb + C::kOffStage + s * C::kStageBytes;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t rr[64];
                 tmem_ld64(tDQ + c * 64, rr);
-                if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 64; e += 4)
-                        red_add_v4(dst + c * 64 + e, __uint_as_float(rr[e]),
-                                   __uint_as_float(rr[e + 1]), __uint_as_float(rr[e + 2]),
-                                   __uint_as_float(rr[e + 3]));
+                for (int hb = 0; hb < 2; ++hb) {          // two 32-column boxes
+                    const uint32_t box = stage + (2 * c + hb) * (kTile * 128) + qr * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const int e = hb * 32 + ch * 4;
+                        st_shared_v4(box + (static_cast<uint32_t>(ch ^ (qr & 7)) << 4), rr[e],
+                                     rr[e + 1], rr[e + 2], rr[e + 3]);
+                    }
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(C::kBarDQEmpty));
+            mbar_arrive(bar(C::kBarDQEmpty));          // TMEM columns of dQ are free
+            fence_proxy_async_smem();
+            named_bar_sync(2, kTile);
+            if (qr == 0) {
+                const int qi = item_qi(j), bhq = item_bhq(j);
+                for (int bx = 0; bx < D / 32; ++bx)
+                    tma_reduce_add_3d(&tmDQ, stage + bx * (kTile * 128), bx * 32, qi * kTile, bhq);
+                tma_store_commit();
+                tma_store_wait_read();
+                mbar_arrive(bar(C::kBarQDEmpty + s));   // stage reusable by the producer
+            }
         }
+        // Hand stage 0 over to the dK/dV epilogue once its last reduction read it.
+        named_bar_sync(3, 2 * kTile);
     } else {
         // ----------------------------------------------- P / dS warpgroup
         const int kr = threadIdx.x;   // key row within the tile == TMEM lane
@@ -386,8 +401,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && (item_qi(j) == kt);
-            const float *lse2 = rows_f + s * kTile;
-            const float *dlt = rows_f + (2 + s) * kTile;
+            const uint32_t s_lse = s_rows + s * kTile * 4;
+            const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4;
+            const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
+            const uint64_t sm2 = f2pack(p.scale, p.scale);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t sr[64], dr[64];
@@ -395,18 +412,30 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tmem_ld64(tDP + h * 64, dr);
                 uint32_t pw[32], dw[32];
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
+                for (int c = 0; c < 64; c += 4) {
                     const int q = h * 64 + c;
-                    float p0 = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -lse2[q]));
-                    float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -lse2[q + 1]));
-                    if (diag) {
-                        p0 = (kr <= q) ? p0 : 0.f;
-                        p1 = (kr <= q + 1) ? p1 : 0.f;
+                    const float4 l4 = ld_shared_f4(s_lse + q * 4);
+                    const float4 d4 = ld_shared_f4(s_dlt + q * 4);
+#pragma unroll
+                    for (int u = 0; u < 4; u += 2) {
+                        const float la = u == 0 ? l4.x : l4.z, lb = u == 0 ? l4.y : l4.w;
+                        const float da = u == 0 ? d4.x : d4.z, db = u == 0 ? d4.y : d4.w;
+                        float t0, t1;
+                        f2unpack(ffma2(f2pack(__uint_as_float(sr[c + u]), __uint_as_float(sr[c + u + 1])),
+                                       sc2, f2pack(-la, -lb)), t0, t1);
+                        float p0 = ex2(t0), p1 = ex2(t1);
+                        if (diag) {
+                            p0 = (kr <= q + u) ? p0 : 0.f;
+                            p1 = (kr <= q + u + 1) ? p1 : 0.f;
+                        }
+                        float e0, e1;   // dP - Delta
+                        f2unpack(fadd2(f2pack(__uint_as_float(dr[c + u]), __uint_as_float(dr[c + u + 1])),
+                                       f2pack(-da, -db)), e0, e1);
+                        float d0, d1;
+                        f2unpack(fmul2(fmul2(f2pack(p0, p1), f2pack(e0, e1)), sm2), d0, d1);
+                        pw[(c + u) >> 1] = pack_bf16x2(p0, p1);
+                        dw[(c + u) >> 1] = pack_bf16x2(d0, d1);
                     }
-                    const float d0 = p0 * (__uint_as_float(dr[c]) - dlt[q]) * p.scale;
-                    const float d1 = p1 * (__uint_as_float(dr[c + 1]) - dlt[q + 1]) * p.scale;
-                    pw[c >> 1] = pack_bf16x2(p0, p1);
-                    dw[c >> 1] = pack_bf16x2(d0, d1);
                 }
                 tmem_st32(tS + h * 32, pw);   // P^T bf16 pairs over columns already read
                 stage_row64(sDS, kr, h, dw);
@@ -419,6 +448,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
         // ------------------------------------------------ epilogue: dK, dV
         if (ok) ok = mbar_wait_warp(bar(C::kBarAccDone), 0, ac);
+        named_bar_sync(3, 2 * kTile);   // the drain is done with the stage buffers
         const uint32_t stV = sb + C::kOffStage;                  // stage 0 Q buffer
         const uint32_t stK = sb + C::kOffStage + C::kTileBytes;  // stage 0 dO buffer
         if (ok) {
@@ -475,13 +505,14 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
 
     // 2. main kernel.
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     if (!encode_bf16_rows(&tq, pb.q, D, pb.N, BH, kTile) ||
         !encode_bf16_rows(&tk, pb.k, D, pb.N, BHkv, kTile) ||
         !encode_bf16_rows(&tv, pb.v, D, pb.N, BHkv, kTile) ||
         !encode_bf16_rows(&tdo, pb.dO, D, pb.N, BH, kTile) ||
         !encode_bf16_rows(&tdk, pb.dk, D, pb.N, BHkv, kTile) ||
-        !encode_bf16_rows(&tdv, pb.dv, D, pb.N, BHkv, kTile))
+        !encode_bf16_rows(&tdv, pb.dv, D, pb.N, BHkv, kTile) ||
+        !encode_f32_rows(&tdq, pb.dq_acc, D, pb.N, BH, kTile))
         return cudaErrorInvalidValue;
     BwdParams prm;
     prm.lse2 = pb.lse2;
@@ -501,7 +532,7 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     auto kern = pb.causal ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, prm);
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

@@ -47,6 +47,9 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int D);
 // swizzle.  Returns false if the driver rejects it.
 bool encode_bf16_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
                       int box_rows);
+// Same for an fp32 [heads, N, D] tensor with a {32, box_rows, 1} box.
+bool encode_f32_rows(CUtensorMap *map, const void *base, int D, int N, long long heads,
+                     int box_rows);
 
 // Device status word of the current device (allocated statically).
 int *device_status_ptr();
