@@ -74,6 +74,8 @@ def source_digest(files):
 
 FWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_fwd.cu",
                "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
+BWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_bwd.cu",
+               "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
 
 
 def profiled_traffic(kernel_tag, digest, units):
@@ -260,12 +262,39 @@ def run_reference(args):
     return 0
 
 
-def config_block(world):
-    W = WORKLOAD
-    return {"workload": W["name"], "B": W["B"], "H": W["Hq"], "Hkv": W["Hkv"], "N": W["N"],
-            "D": W["D"], "causal": W["causal"], "scale": 1 / math.sqrt(W["D"]),
-            "parallelism": f"replicas x{world} (independent problems, no collective)",
-            "l2": "flushed between timed steps (256 MB write)"}
+def config_block(world, W=None):
+    W = W or WORKLOAD
+    cfg = {"workload": W["name"], "B": W["B"], "H": W["Hq"], "Hkv": W["Hkv"], "N": W["N"],
+           "D": W["D"], "causal": W["causal"], "scale": 1 / math.sqrt(W["D"]),
+           "parallelism": f"replicas x{world} (independent problems, no collective)",
+           "l2": "flushed between timed steps (256 MB write)"}
+    if W.get("kind") == "chain":
+        cfg["layers"] = W["layers"]
+    return cfg
+
+
+# Optional workloads for manual measurement (the default line is WORKLOAD).
+EXTRA_WORKLOADS = {
+    "noncausal_fwd": dict(name="noncausal_fwd_B8_H32_N2048_D128", kind="fwd", B=8, Hq=32,
+                          Hkv=32, N=2048, D=128, causal=False),
+    "causal_fwd_d64": dict(name="causal_fwd_B2_H16_N4096_D64", kind="fwd", B=2, Hq=16, Hkv=16,
+                           N=4096, D=64, causal=True),
+    "residual_chain": dict(name="residual_chain_4layers_B1_H20_KV4_N4096_D128", kind="chain",
+                           layers=4, B=1, Hq=20, Hkv=4, N=4096, D=128, causal=True),
+    "tiny": dict(name="tiny_fwd_B1_H1_N128_D64", kind="fwd", B=1, Hq=1, Hkv=1, N=128, D=64,
+                 causal=False),
+}
+
+
+def chain_layer_bytes(W, layer):
+    """Algorithmic HBM bytes of one chained layer: Q, K, V read, O and LSE
+    written, plus the kept (j <= i under the causal mask) fp32 logits read
+    from the previous layer (layers 1..L-1) and written for the next (layers
+    0..L-2)."""
+    B, Hq, Hkv, N, D, L = W["B"], W["Hq"], W["Hkv"], W["N"], W["D"], W["layers"]
+    kept = N * (N + 1) // 2 if W["causal"] else N * N
+    base = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+    return base + (layer > 0) * B * Hq * kept * 4 + (layer < L - 1) * B * Hq * kept * 4
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -276,52 +305,87 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import tiled_attention_02_gb300 as ta
-    from tiled_attention_02_gb300.inputs import make_qkv
+    from tiled_attention_02_gb300.inputs import make_chain, make_qkv
     ta.build()
-    W = WORKLOAD
+    W = WORKLOAD if args.workload == "step" else EXTRA_WORKLOADS[args.workload]
+    kind = W.get("kind", "fwd_bwd")
     B, Hq, Hkv, N, D, causal = W["B"], W["Hq"], W["Hkv"], W["N"], W["D"], W["causal"]
     scale = 1.0 / math.sqrt(D)
-    x = make_qkv(B, Hq, Hkv, N, D, seed=rank, with_do=True)
-    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
-    o = torch.empty_like(q)
-    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256), dtype=torch.uint8,
-                     device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # Does this build have the backward?
-    st = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                         lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                         dv.data_ptr(), 1, 1, 1, 128, D, scale, 1, ws.data_ptr(),
-                         ws.numel(), sh)
-    have_bwd = (st == ta.ATTN_OK)
-    torch.cuda.synchronize(dev)
+    # phases: list of (label, fn, flops, algorithmic bytes) run in order per step
+    phases = []
+    host_inputs, dev_inputs, results = [], [], []
+    if kind == "chain":
+        layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
+        dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
+        outs = [(torch.empty_like(x["q"]),
+                 torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
+        buf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
+        L = W["layers"]
+        for i in range(L):
+            def layer(i=i):
+                x, (o, lse) = dl[i], outs[i]
+                s = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                    buf.data_ptr() if i > 0 else None, o.data_ptr(),
+                                    lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                    buf.data_ptr() if i < L - 1 else None, sh)
+                assert s == 0, s
+            phases.append((f"layer{i}", layer, attn_flops(B, Hq, N, D, causal),
+                           chain_layer_bytes(W, i)))
+        for i, x in enumerate(layers):
+            for n in ("q", "k", "v"):
+                host_inputs.append(x[n])
+                dev_inputs.append(dl[i][n])
+        results = [outs[-1][0]]
+    else:
+        x = make_qkv(B, Hq, Hkv, N, D, seed=rank, with_do=(kind == "fwd_bwd"))
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
 
-    def fwd():
-        s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, o.data_ptr(),
-                            lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal, None, sh)
-        assert s == 0, s
+        def fwd():
+            s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, o.data_ptr(),
+                                lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal, None, sh)
+            assert s == 0, s
+        io_bytes = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+        phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal), io_bytes))
+        host_inputs += [x["q"], x["k"], x["v"]]
+        dev_inputs += [q, k, v]
+        results = [o]
+        if kind == "fwd_bwd":
+            do = x["do"].to(dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+                             dtype=torch.uint8, device=dev)
 
-    def bwd():
-        s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                            dv.data_ptr(), B, Hq, Hkv, N, D, scale, causal, ws.data_ptr(),
-                            ws.numel(), sh)
-        assert s == 0, s
+            def bwd():
+                s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                    ws.data_ptr(), ws.numel(), sh)
+                assert s == 0, s
+            bwd_bytes = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+            phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal), bwd_bytes))
+            host_inputs.append(x["do"])
+            dev_inputs.append(do)
+            results = [dq, dk, dv]
+    launches = {"fwd": 1, "bwd": 3}
+    launches_per_step = sum(launches.get(lbl, 1) for lbl, *_ in phases)
 
-    launches_per_step = 1 + (3 if have_bwd else 0)
+    def step():
+        for _, fn, _, _ in phases:
+            fn()
+
     for _ in range(args.warmup):
-        fwd()
-        if have_bwd:
-            bwd()
+        step()
     torch.cuda.synchronize(dev)
     assert ta.attn_last_device_status() == 0
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    gpu_id = None
+    nph = len(phases)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     try:
         gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
         if not gpu_id.startswith("GPU-"):
@@ -336,51 +400,37 @@ def run_ours(args):
     for i in range(args.steps):
         flush.fill_(float(i))       # untimed: evicts the previous step's data from L2
         ev[i][0].record(stream)
-        fwd()
-        ev[i][1].record(stream)
-        if have_bwd:
-            bwd()
-        ev[i][2].record(stream)
+        for j, (_, fn, _, _) in enumerate(phases):
+            fn()
+            ev[i][j + 1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
     status = ta.attn_last_device_status()
     assert status == 0, ta.attn_status_string(status)
 
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if have_bwd else [0.0] * args.steps
-    step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
-    ms_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
-    fwd_avg = max_over_ranks(sum(fwd_ms) / len(fwd_ms), world, dev)
-    bwd_avg = max_over_ranks(sum(bwd_ms) / len(bwd_ms), world, dev) if have_bwd else 0.0
-    f_fwd = attn_flops(B, Hq, N, D, causal)
-    f_bwd = bwd_flops(B, Hq, N, D, causal) if have_bwd else 0.0
-    flops_step = f_fwd + f_bwd
+    ph_ms = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(nph)]
+    ph_avg = [max_over_ranks(sum(t) / len(t), world, dev) for t in ph_ms]
+    ms_step = max_over_ranks(sum(sum(e[j].elapsed_time(e[j + 1]) for j in range(nph)) for e in ev)
+                             / args.steps, world, dev)
+    flops_step = sum(ph[2] for ph in phases)
+    bytes_step = sum(ph[3] for ph in phases)
     value = world * flops_step / (ms_step * 1e-3) / 1e12
 
     # ------------------------------------------------------------ e2e
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
-        outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
-                for t in ((dq, dk, dv) if have_bwd else (o,))]
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hdo,) if have_bwd else ()))
-        d2h = sum(t.numel() * t.element_size() for t in outs)
+        pinned = [t.pin_memory() for t in host_inputs]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
+        h2d = sum(t.numel() * t.element_size() for t in pinned)
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
         def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            if have_bwd:
-                do.copy_(hdo, non_blocking=True)
-            fwd()
-            if have_bwd:
-                bwd()
-                outs[0].copy_(dq, non_blocking=True)
-                outs[1].copy_(dk, non_blocking=True)
-                outs[2].copy_(dv, non_blocking=True)
-            else:
-                outs[0].copy_(o, non_blocking=True)
+            for d, h in zip(dev_inputs, pinned):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(outs_h, results):
+                h.copy_(d, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -398,30 +448,56 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ------------------------------------------------------- roofline
+    # The dominant kernel by device time decides the roofline entry; every
+    # phase is reported under "kernels".
     pk = peaks()
     n_qt = (N + 127) // 128
     units = B * Hq * (n_qt * (n_qt + 1) // 2 if causal else n_qt * n_qt)   # 128x128 tile pairs
-    digest = source_digest(FWD_SOURCES)
-    achieved = f_fwd / (fwd_avg * 1e-3) / 1e12
-    roof = {"kernel": "fwd_kernel<128,causal>", "bound": "tensor", "achieved": achieved,
-            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-            "peak_source": f"{pk['source']} bf16 burst",
-            "traffic": profiled_traffic("fwd_kernel_causal_B1_H16_N16384_D128", digest, units),
-            "flops_per_launch": f_fwd, "units_per_launch": units,
-            "avg_launch_ms": fwd_avg, "source_digest": digest}
+    tag = f"{'causal' if causal else 'noncausal'}_B{B}_H{Hq}_N{N}_D{D}"
+    kernels = {}
+    for (lbl, _, fl, by), avg in zip(phases, ph_avg):
+        if kind == "chain":
+            dg = source_digest(FWD_SOURCES)
+            ach = by / (avg * 1e-3) / 1e9
+            kernels[lbl] = {"kernel": f"fwd_kernel<{D},causal,bias/emit>", "bound": "hbm",
+                            "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                            "frac": ach / pk["hbm_gbs"],
+                            "traffic": profiled_traffic(f"fwd_kernel_chain_{tag}", dg, units),
+                            "bytes_per_launch": by, "flops_per_launch": fl,
+                            "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
+                            "launches_timed": 1, "source_digest": dg}
+            continue
+        is_bwd = lbl == "bwd"
+        dg = source_digest(BWD_SOURCES if is_bwd else FWD_SOURCES)
+        ach = fl / (avg * 1e-3) / 1e12
+        name = f"{'bwd_main_kernel' if is_bwd else 'fwd_kernel'}_{tag}"
+        kernels[lbl] = {"kernel": f"{'bwd_main_kernel' if is_bwd else 'fwd_kernel'}<{D},"
+                                  f"{'causal' if causal else 'noncausal'}>",
+                        "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
+                        "traffic": profiled_traffic(name, dg, units),
+                        "flops_per_launch": fl, "units_per_launch": units,
+                        "avg_launch_ms": avg, "launches_timed": 3 if is_bwd else 1,
+                        "source_digest": dg}
+        if is_bwd:
+            kernels[lbl]["timing_note"] = ("CUDA events around attn_bwd: preprocess + main + "
+                                           "dQ convert; the main kernel dominates (ncu launch list)")
+    dom = max(kernels, key=lambda kk: kernels[kk]["avg_launch_ms"])
+    roof = dict(kernels[dom])
+    roof["peak_source"] = (f"{pk['source']} HBM copy" if roof["bound"] == "hbm"
+                           else f"{pk['source']} bf16 burst")
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic: q,k,v,dO ~ N(0,1) bf16, seeded",
-            "config": dict(config_block(world),
-                           step="forward + backward" if have_bwd else
-                           "forward only (backward not in this build)"),
-            "fwd_tflops": f_fwd / (fwd_avg * 1e-3) / 1e12,
-            "bwd_tflops": (f_bwd / (bwd_avg * 1e-3) / 1e12) if have_bwd else None,
+            "data": "synthetic: q,k,v(,dO) ~ N(0,1) bf16, seeded",
+            "config": dict(config_block(world, W),
+                           step={"fwd_bwd": "forward + backward", "fwd": "forward",
+                                 "chain": "four chained forward layers, fp32 residual in place"}[kind]),
             "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
-            "roofline": roof, "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
-            "e2e": e2e}
+            "hbm_gbs_step": world * bytes_step / (ms_step * 1e-3) / 1e9,
+            "roofline": roof, "kernels": kernels, "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps, "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_min_s, args.cpu_max_s)
     if rank == 0:
@@ -438,6 +514,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="step", choices=["step", *EXTRA_WORKLOADS],
+                    help="step (default): the causal fwd+bwd line; others for manual runs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-min-s", type=float, default=10.0)
