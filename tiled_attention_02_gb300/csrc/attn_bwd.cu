@@ -27,11 +27,13 @@
 //                       query heads of a kv group) and are stored once.
 //  3. bwd_dq_kernel     fp32 dQ accumulator -> bf16 dQ.
 //
-// Warp roles of the main kernel (320 threads, one CTA per SM):
-//   warps 0-3  thread r owns key row r: P^T, dS^T; epilogue of dK, dV.
-//   warps 4-7  thread r owns query row r of the dQ tile: TMEM -> smem -> TMA add.
-//   warp 8     TMA producer (K, V once; Q, dO, LSE, Delta per query tile).
-//   warp 9     TMEM allocator and tcgen05.mma issuer.
+// Warp roles of the main kernel (448 threads, one CTA per SM):
+//   warps 0-7  two warpgroups; warpgroup w computes P^T and dS^T for query
+//              columns 64w..64w+63 (thread r = key row r = TMEM lane r);
+//              epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK.
+//   warps 8-11 thread r owns query row r of the dQ tile: TMEM -> smem -> TMA add.
+//   warp 12    TMA producer (K, V once; Q, dO, LSE, Delta per query tile).
+//   warp 13    TMEM allocator and tcgen05.mma issuer.
 // TMEM columns: S^T/P^T 0..127, dP^T/dQ 128..255, dV 256.., dK 256+D...
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
@@ -107,7 +109,7 @@ bwd_dq_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, siz
 
 // ------------------------------------------------------------ main kernel
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kMaxSmem = 232448;   // opt-in shared memory per block on sm_100/sm_103
 
 template <int D>
@@ -223,7 +225,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(C::kBarQDEmpty + s), 1);
         }
         mbar_init(bar(C::kBarSFull), 1);
-        mbar_init(bar(C::kBarPReady), kTile);
+        mbar_init(bar(C::kBarPReady), 2 * kTile);
         mbar_init(bar(C::kBarDQFull), 1);
         mbar_init(bar(C::kBarDQEmpty), kTile);
         mbar_init(bar(C::kBarDSFree), 1);
@@ -231,7 +233,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -240,7 +242,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             bool ok = true;
@@ -277,7 +279,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, false, false);
@@ -311,7 +313,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {   // dV += P^T dO  (A in TMEM)
-                    mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                    // P^T of query columns 64w..64w+63 sits in TMEM columns
+                    // 64w..64w+31 (over warpgroup w's own, already read, S^T).
+                    mma_ts(tmem + C::kColDV, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                            sdesc_sw128(sdO + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -339,15 +343,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 8) {
         // ------------------------------------------------ dQ drain warpgroup
         // dQ(j) is staged (fp32, 128-byte swizzled boxes of 32 columns) in the
         // Q/dO buffers of item j's stage -- exactly 128 x D x 4 bytes, free
         // once item j's MMAs are done -- and added into the fp32 accumulator
         // with TMA bulk reductions.  The stage is handed back to the producer
         // only after the reductions have read it.
-        const int qr = threadIdx.x - 128;
-        const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16) + C::kColDP;
+        const int qr = threadIdx.x - 256;
+        const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 8) * 32) << 16) + C::kColDP;
         for (int j = 0; j < n_items; ++j) {
             const int s = j & 1;
             const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
@@ -384,14 +388,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
         // Hand stage 0 over to the dK/dV epilogue once its last reduction read it.
-        named_bar_sync(3, 2 * kTile);
+        named_bar_sync(3, 3 * kTile);
     } else {
-        // ----------------------------------------------- P / dS warpgroup
-        const int kr = threadIdx.x;   // key row within the tile == TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS;
-        const uint32_t tDP = tmem + lane_base + C::kColDP;
+        // ---------------------------------------- two P / dS warpgroups
+        // Warpgroup w (warps 4w..4w+3) owns query columns 64w..64w+63; thread
+        // kr is key row kr (TMEM lane kr).
+        const int w = warp >> 2;
+        const int kr = threadIdx.x & 127;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::kColS + w * 64;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + w * 64;
         const uint32_t sDS = sb + C::kOffDS;
+        const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
+        const uint64_t sm2 = f2pack(p.scale, p.scale);
         bool ok = true;
         for (int j = 0; j < n_items; ++j) {
             const int s = j & 1;
@@ -401,45 +410,50 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && (item_qi(j) == kt);
-            const uint32_t s_lse = s_rows + s * kTile * 4;
-            const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4;
-            const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
-            const uint64_t sm2 = f2pack(p.scale, p.scale);
+            const uint32_t s_lse = s_rows + s * kTile * 4 + w * 256;
+            const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4 + w * 256;
+            uint32_t pw[32];   // P^T of this warpgroup's 64 columns, bf16 pairs
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sr[64], dr[64];
-                tmem_ld64(tS + h * 64, sr);
-                tmem_ld64(tDP + h * 64, dr);
-                uint32_t pw[32], dw[32];
+            for (int h = 0; h < 2; ++h) {   // 32 columns at a time
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tS + h * 32, sr);
+                tmem_ld32(tDP + h * 32, dr);
 #pragma unroll
-                for (int c = 0; c < 64; c += 4) {
-                    const int q = h * 64 + c;
-                    const float4 l4 = ld_shared_f4(s_lse + q * 4);
-                    const float4 d4 = ld_shared_f4(s_dlt + q * 4);
+                for (int c = 0; c < 32; c += 8) {   // one 16-byte chunk of the dS^T row
+                    const int cc = h * 32 + c;      // column within this warpgroup's 64
+                    const float4 la = ld_shared_f4(s_lse + cc * 4);
+                    const float4 lb = ld_shared_f4(s_lse + cc * 4 + 16);
+                    const float4 da = ld_shared_f4(s_dlt + cc * 4);
+                    const float4 db = ld_shared_f4(s_dlt + cc * 4 + 16);
+                    const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+                    const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+                    uint32_t wv[4];
 #pragma unroll
-                    for (int u = 0; u < 4; u += 2) {
-                        const float la = u == 0 ? l4.x : l4.z, lb = u == 0 ? l4.y : l4.w;
-                        const float da = u == 0 ? d4.x : d4.z, db = u == 0 ? d4.y : d4.w;
+                    for (int u = 0; u < 8; u += 2) {
                         float t0, t1;
                         f2unpack(ffma2(f2pack(__uint_as_float(sr[c + u]), __uint_as_float(sr[c + u + 1])),
-                                       sc2, f2pack(-la, -lb)), t0, t1);
+                                       sc2, f2pack(-lv[u], -lv[u + 1])), t0, t1);
                         float p0 = ex2(t0), p1 = ex2(t1);
                         if (diag) {
-                            p0 = (kr <= q + u) ? p0 : 0.f;
-                            p1 = (kr <= q + u + 1) ? p1 : 0.f;
+                            const int q = w * 64 + cc + u;
+                            p0 = (kr <= q) ? p0 : 0.f;
+                            p1 = (kr <= q + 1) ? p1 : 0.f;
                         }
                         float e0, e1;   // dP - Delta
                         f2unpack(fadd2(f2pack(__uint_as_float(dr[c + u]), __uint_as_float(dr[c + u + 1])),
-                                       f2pack(-da, -db)), e0, e1);
+                                       f2pack(-dv[u], -dv[u + 1])), e0, e1);
                         float d0, d1;
                         f2unpack(fmul2(fmul2(f2pack(p0, p1), f2pack(e0, e1)), sm2), d0, d1);
-                        pw[(c + u) >> 1] = pack_bf16x2(p0, p1);
-                        dw[(c + u) >> 1] = pack_bf16x2(d0, d1);
+                        pw[(cc + u) >> 1] = pack_bf16x2(p0, p1);
+                        wv[u >> 1] = pack_bf16x2(d0, d1);
                     }
+                    const int chunk = cc >> 3;     // 16-byte chunk within the 64-query atom
+                    st_shared_v4(sDS + w * (kTile * 128) + kr * 128 +
+                                     (static_cast<uint32_t>(chunk ^ (kr & 7)) << 4),
+                                 wv[0], wv[1], wv[2], wv[3]);
                 }
-                tmem_st32(tS + h * 32, pw);   // P^T bf16 pairs over columns already read
-                stage_row64(sDS, kr, h, dw);
             }
+            tmem_st32(tS, pw);   // columns 64w..64w+31, already read
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -447,31 +461,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
 
         // ------------------------------------------------ epilogue: dK, dV
+        // Warpgroup 0 stores dV, warpgroup 1 stores dK (all D columns of each key row).
         if (ok) ok = mbar_wait_warp(bar(C::kBarAccDone), 0, ac);
-        named_bar_sync(3, 2 * kTile);   // the drain is done with the stage buffers
+        named_bar_sync(3, 3 * kTile);   // the drain is done with the stage buffers
         const uint32_t stV = sb + C::kOffStage;                  // stage 0 Q buffer
         const uint32_t stK = sb + C::kOffStage + C::kTileBytes;  // stage 0 dO buffer
         if (ok) {
             tc_fence_after();
+            const uint32_t col = w == 0 ? C::kColDV : C::kColDK;
+            const uint32_t dst = w == 0 ? stV : stK;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
-                const uint32_t dst = which == 0 ? stV : stK;
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t rr[64];
+                tmem_ld64(tmem + lane_base + col + c * 64, rr);
+                uint32_t wv[32];
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t rr[64];
-                    tmem_ld64(tmem + lane_base + col + c * 64, rr);
-                    uint32_t w[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                    stage_row64(dst, kr, c, w);
-                }
+                for (int e = 0; e < 32; ++e)
+                    wv[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                stage_row64(dst, kr, c, wv);
             }
             fence_proxy_async_smem();
         }
         tc_fence_before();
-        named_bar_sync(1, kTile);
+        named_bar_sync(1, 2 * kTile);
         if (threadIdx.x == 0 && *abort_flag == 0) {
             for (int c = 0; c < C::kChunks; ++c) {
                 tma_store_3d(&tmdV, stV + c * C::kChunkBytes, c * 64, kt * kTile, bh_kv);
@@ -484,7 +496,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
