@@ -35,6 +35,8 @@
 //   warp 12    TMA producer (K, V once; Q, dO, LSE, Delta per query tile).
 //   warp 13    TMEM allocator and tcgen05.mma issuer.
 // TMEM columns: S^T/P^T 0..127, dP^T/dQ 128..255, dV 256.., dK 256+D...
+// MMA order per query tile j: S^T(j), dP^T(j), dV(j), dK(j), dQ(j); the P^T
+// work overlaps dP^T and the dS^T work overlaps dV.
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -129,13 +131,15 @@ struct BwdCfg {
     static constexpr int kBarQDFull = 1;     // 2
     static constexpr int kBarQDEmpty = 3;    // 2
     static constexpr int kBarSFull = 5;
-    static constexpr int kBarPReady = 6;
-    static constexpr int kBarDQFull = 7;
-    static constexpr int kBarDQEmpty = 8;
-    static constexpr int kBarDSFree = 9;
-    static constexpr int kBarAccDone = 10;
-    static constexpr int kBarDrain = 11;
-    static constexpr int kNumBars = 12;
+    static constexpr int kBarDPFull = 6;
+    static constexpr int kBarPReady = 7;
+    static constexpr int kBarDSReady = 8;
+    static constexpr int kBarDQFull = 9;
+    static constexpr int kBarDQEmpty = 10;
+    static constexpr int kBarDSFree = 11;
+    static constexpr int kBarAccDone = 12;
+    static constexpr int kBarDrain = 13;
+    static constexpr int kNumBars = 14;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kUsed = kOffMisc + 16;
     static constexpr int kSmemBytes = (kUsed + 1023 <= kMaxSmem) ? kUsed + 1023 : kMaxSmem;
@@ -225,7 +229,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(C::kBarQDEmpty + s), 1);
         }
         mbar_init(bar(C::kBarSFull), 1);
+        mbar_init(bar(C::kBarDPFull), 1);
         mbar_init(bar(C::kBarPReady), 2 * kTile);
+        mbar_init(bar(C::kBarDSReady), 2 * kTile);
         mbar_init(bar(C::kBarDQFull), 1);
         mbar_init(bar(C::kBarDQEmpty), kTile);
         mbar_init(bar(C::kBarDSFree), 1);
@@ -287,29 +293,33 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, D, true, true);     // dQ
             bool ok = mbar_wait(bar(C::kBarKV), 0, ac);
             for (int j = 0; j < n_items && ok; ++j) {
+                // Order per query tile j:
+                //   S^T(j)  dP^T(j)  [P_ready] dV(j)  [dS_ready] dK(j)  dQ(j)
+                // P is computed while dP^T runs and dS while dV runs.
                 const int s = j & 1;
-                ok = mbar_wait(bar(C::kBarQDFull + s), (j >> 1) & 1, ac);
-                if (ok && j > 0) ok = mbar_wait(bar(C::kBarDQEmpty), (j - 1) & 1, ac);
-                if (!ok) break;
+                if (!(ok = mbar_wait(bar(C::kBarQDFull + s), (j >> 1) & 1, ac))) break;
                 tc_fence_after();
                 const uint32_t sQ = sb + C::kOffStage + s * C::kStageBytes;
                 const uint32_t sdO = sQ + C::kTileBytes;
                 const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV, sDS = sb + C::kOffDS;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T
+                for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T (over P^T(j-1), read by dV(j-1))
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024),
                            sdesc_sw128(sQ + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
+                mma_commit(bar(C::kBarSFull));
+                // dP^T overwrites dQ(j-1): the drain must have read it.
+                if (j > 0 && !(ok = mbar_wait(bar(C::kBarDQEmpty), (j - 1) & 1, ac))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {   // dP^T = V dO^T
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024),
                            sdesc_sw128(sdO + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(C::kBarSFull));
-                ok = mbar_wait(bar(C::kBarPReady), j & 1, ac);
-                if (!ok) break;
+                mma_commit(bar(C::kBarDPFull));
+                if (!(ok = mbar_wait(bar(C::kBarPReady), j & 1, ac))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {   // dV += P^T dO  (A in TMEM)
@@ -319,6 +329,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                            sdesc_sw128(sdO + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
+                if (!(ok = mbar_wait(bar(C::kBarDSReady), j & 1, ac))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {   // dK += dS^T Q
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -332,7 +344,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                            sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), kIdDQ,
                            kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(C::kBarDQFull));
+                mma_commit(bar(C::kBarDQFull));   // also: every MMA of item j has completed
                 mma_commit(bar(C::kBarDSFree));
             }
             if (ok) {
@@ -404,9 +416,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         for (int j = 0; j < n_items; ++j) {
             const int s = j & 1;
+            // --- P^T(j) = 2^(S^T scale log2e - LSE log2e), bf16 into TMEM over S^T
             ok = mbar_wait_warp(bar(C::kBarSFull), j & 1, ac);
             if (ok) ok = mbar_wait_warp(bar(C::kBarQDFull + s), (j >> 1) & 1, ac);
-            if (ok && j > 0) ok = mbar_wait_warp(bar(C::kBarDSFree), (j - 1) & 1, ac);
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && (item_qi(j) == kt);
@@ -414,37 +426,60 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4 + w * 256;
             uint32_t pw[32];   // P^T of this warpgroup's 64 columns, bf16 pairs
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {   // 32 columns at a time
-                uint32_t sr[32], dr[32];
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sr[32];
                 tmem_ld32(tS + h * 32, sr);
-                tmem_ld32(tDP + h * 32, dr);
 #pragma unroll
-                for (int c = 0; c < 32; c += 8) {   // one 16-byte chunk of the dS^T row
-                    const int cc = h * 32 + c;      // column within this warpgroup's 64
-                    const float4 la = ld_shared_f4(s_lse + cc * 4);
-                    const float4 lb = ld_shared_f4(s_lse + cc * 4 + 16);
-                    const float4 da = ld_shared_f4(s_dlt + cc * 4);
-                    const float4 db = ld_shared_f4(s_dlt + cc * 4 + 16);
-                    const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-                    const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-                    uint32_t wv[4];
+                for (int c = 0; c < 32; c += 4) {
+                    const int cc = h * 32 + c;
+                    const float4 l4 = ld_shared_f4(s_lse + cc * 4);
 #pragma unroll
-                    for (int u = 0; u < 8; u += 2) {
+                    for (int u = 0; u < 4; u += 2) {
+                        const float la = u == 0 ? l4.x : l4.z, lb = u == 0 ? l4.y : l4.w;
                         float t0, t1;
                         f2unpack(ffma2(f2pack(__uint_as_float(sr[c + u]), __uint_as_float(sr[c + u + 1])),
-                                       sc2, f2pack(-lv[u], -lv[u + 1])), t0, t1);
+                                       sc2, f2pack(-la, -lb)), t0, t1);
                         float p0 = ex2(t0), p1 = ex2(t1);
                         if (diag) {
                             const int q = w * 64 + cc + u;
                             p0 = (kr <= q) ? p0 : 0.f;
                             p1 = (kr <= q + 1) ? p1 : 0.f;
                         }
+                        pw[(cc + u) >> 1] = pack_bf16x2(p0, p1);
+                    }
+                }
+            }
+            tmem_st32(tS, pw);   // columns 64w..64w+31, already read
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarPReady));
+
+            // --- dS^T(j) = P^T o (dP^T - Delta) * scale, bf16 into smem
+            ok = mbar_wait_warp(bar(C::kBarDPFull), j & 1, ac);
+            if (ok && j > 0) ok = mbar_wait_warp(bar(C::kBarDSFree), (j - 1) & 1, ac);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t dr[32];
+                tmem_ld32(tDP + h * 32, dr);
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {   // one 16-byte chunk of the dS^T row
+                    const int cc = h * 32 + c;
+                    const float4 da = ld_shared_f4(s_dlt + cc * 4);
+                    const float4 db = ld_shared_f4(s_dlt + cc * 4 + 16);
+                    const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int u = 0; u < 8; u += 2) {
                         float e0, e1;   // dP - Delta
                         f2unpack(fadd2(f2pack(__uint_as_float(dr[c + u]), __uint_as_float(dr[c + u + 1])),
                                        f2pack(-dv[u], -dv[u + 1])), e0, e1);
+                        // P as rounded to bf16 for the dV MMA (the same values in both).
+                        const float2 pp = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162 *>(&pw[(cc + u) >> 1]));
                         float d0, d1;
-                        f2unpack(fmul2(fmul2(f2pack(p0, p1), f2pack(e0, e1)), sm2), d0, d1);
-                        pw[(cc + u) >> 1] = pack_bf16x2(p0, p1);
+                        f2unpack(fmul2(fmul2(f2pack(pp.x, pp.y), f2pack(e0, e1)), sm2), d0, d1);
                         wv[u >> 1] = pack_bf16x2(d0, d1);
                     }
                     const int chunk = cc >> 3;     // 16-byte chunk within the 64-query atom
@@ -453,11 +488,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                  wv[0], wv[1], wv[2], wv[3]);
                 }
             }
-            tmem_st32(tS, pw);   // columns 64w..64w+31, already read
-            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(C::kBarPReady));
+            mbar_arrive(bar(C::kBarDSReady));
         }
 
         // ------------------------------------------------ epilogue: dK, dV
