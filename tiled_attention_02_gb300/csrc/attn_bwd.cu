@@ -425,14 +425,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t s_lse = s_rows + s * kTile * 4 + w * 256;
             const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4 + w * 256;
             uint32_t pw[32];   // P^T of this warpgroup's 64 columns, bf16 pairs
+            {
+                uint32_t sr[64];
+                tmem_ld64(tS, sr);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sr[32];
-                tmem_ld32(tS + h * 32, sr);
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const int cc = h * 32 + c;
-                    const float4 l4 = ld_shared_f4(s_lse + cc * 4);
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 l4 = ld_shared_f4(s_lse + c * 4);
 #pragma unroll
                     for (int u = 0; u < 4; u += 2) {
                         const float la = u == 0 ? l4.x : l4.z, lb = u == 0 ? l4.y : l4.w;
@@ -441,11 +439,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                        sc2, f2pack(-la, -lb)), t0, t1);
                         float p0 = ex2(t0), p1 = ex2(t1);
                         if (diag) {
-                            const int q = w * 64 + cc + u;
+                            const int q = w * 64 + c + u;
                             p0 = (kr <= q) ? p0 : 0.f;
                             p1 = (kr <= q + 1) ? p1 : 0.f;
                         }
-                        pw[(cc + u) >> 1] = pack_bf16x2(p0, p1);
+                        pw[(c + u) >> 1] = pack_bf16x2(p0, p1);
                     }
                 }
             }
