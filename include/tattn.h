@@ -81,8 +81,11 @@ typedef enum {
  *   bias         fp32 [B,Hq,N,N]   additive logit bias, or NULL     (in)
  *                Added, unscaled, to scale*QK^T before the mask and the
  *                softmax (the previous layer's pre-softmax logits in a
- *                block attention residual).  Under the causal mask only
- *                entries with j <= i are read.
+ *                block attention residual).  Under the causal mask the
+ *                entries with j > i do not affect any result; the 128 x 128
+ *                tiles strictly above the diagonal are never read, while
+ *                entries above the diagonal inside the tiles that straddle
+ *                it may be read.
  *   o            bf16 [B,Hq,N,D]   output, rounded to nearest even  (out)
  *   lse          fp32 [B,Hq,N]     LSE_i = m_i + ln l_i over the scaled,
  *                biased, masked logits (natural log), or NULL       (out)

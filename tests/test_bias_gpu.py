@@ -38,6 +38,9 @@ CASES = [
     (2, 2, 1, 256, 64, True),
     (1, 2, 2, 203, 64, False),     # N % 4 != 0: scalar bias path, ragged tail
     (1, 3, 3, 130, 128, True),
+    (1, 2, 1, 260, 128, True),     # N % 32 != 0: ragged inside a staged fp32 chunk
+    (1, 2, 2, 260, 128, False),
+    (1, 2, 1, 640, 64, True),      # five key tiles: the staged ring wraps
 ]
 
 
@@ -95,6 +98,57 @@ def test_in_place_alias(ta, orc):
     ref = orc.forward(*orc_in(x), scale=1 / 8, causal=True, bias=bias.numpy(), emit_logits=True)
     check_o(o, ref["o"], "alias")
     check_logits(buf, ref["logits"], "alias")
+
+
+def test_staged_and_direct_paths_agree(ta):
+    """Bias and emit rows that are 16-byte aligned go through the staged
+    (TMA) path; the same values one float off a 16-byte boundary go through
+    the direct per-thread path.  Both evaluate y = fma(qk, scale, bias) on the
+    same accumulator, so O, LSE and every kept logit agree bit for bit."""
+    B, Hq, Hkv, N, D = 1, 2, 1, 384, 128
+    x = make_qkv(B, Hq, Hkv, N, D, seed=31)
+    bias = make_bias(B, Hq, N, seed=32).cuda()
+    q, k, v = dev(x)
+    n = bias.numel()
+    raw_b = torch.empty(n + 4, device="cuda")
+    raw_e = torch.full((n + 4,), float("nan"), device="cuda")
+    b_off = raw_b[1:n + 1].view(B, Hq, N, N)
+    e_off = raw_e[1:n + 1].view(B, Hq, N, N)
+    b_off.copy_(bias)
+    assert b_off.data_ptr() % 16 == 4
+    e_al = torch.full_like(bias, float("nan"))
+    for causal in (True, False):
+        o1, l1 = ta.attn_fwd(q, k, v, bias, causal=causal, emit_logits=e_al)
+        o2, l2 = ta.attn_fwd(q, k, v, b_off, causal=causal, emit_logits=e_off)
+        torch.cuda.synchronize()
+        assert ta.attn_last_device_status() == 0
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        keep = torch.ones(N, N, dtype=torch.bool, device="cuda")
+        if causal:
+            keep = torch.tril(keep)
+        assert torch.equal(e_al[..., keep], e_off[..., keep])
+
+
+def test_causal_emit_leaves_upper_tiles(ta):
+    """Under the causal mask the 128 x 128 logit tiles strictly above the
+    diagonal are never written (both residual paths)."""
+    B, Hq, Hkv, N, D = 1, 2, 2, 384, 64
+    x = make_qkv(B, Hq, Hkv, N, D, seed=41)
+    q, k, v = dev(x)
+    sentinel = 12345.0
+    for off in (0, 1):   # 0: staged path, 1: direct path (misaligned rows)
+        raw = torch.full((B * Hq * N * N + 4,), sentinel, device="cuda")
+        emit = raw[off:off + B * Hq * N * N].view(B, Hq, N, N)
+        ta.attn_fwd(q, k, v, causal=True, emit_logits=emit)
+        torch.cuda.synchronize()
+        assert ta.attn_last_device_status() == 0
+        for qt in range(3):
+            for kt in range(3):
+                blk = emit[..., qt * 128:(qt + 1) * 128, kt * 128:(kt + 1) * 128]
+                if kt > qt:
+                    assert bool((blk == sentinel).all()), (off, qt, kt)
+                else:
+                    assert bool(torch.isfinite(blk).all())
 
 
 def test_zero_bias_equals_no_bias(ta):

@@ -18,14 +18,29 @@
 // (Block Attention Residual Triton kernel, "v1: Fuse Residual 进 Attention
 // Kernel").  exp is evaluated as 2^x with the scale folded in.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (one CTA per SM):
 //   warps 0-3  softmax: thread r owns query row r (TMEM lane r); also the
 //              O rescale and the epilogue.
-//   warp 4     TMA producer: Q once, then K_j / V_j through 2-3 stage rings.
+//   warp 4     TMA producer: Q once, then K_j / V_j through 1-3 stage rings.
 //   warp 5     TMEM allocator and single-thread tcgen05.mma issuer.
+//   warps 6-7  (staged residual only) fp32 bias loader and emitted-logit
+//              storer, see below.
 // TMEM (512 columns): S/P double buffer at columns 0 and 128, O at 256.
 // Issue order on the tensor core: S_0, S_1, PV_0, S_2, PV_1, ... so that the
 // softmax of tile j overlaps the MMAs of tiles j+1 and j-1.
+//
+// The residual variants (bias and/or emitted logits) move 2 x 64 KB of fp32
+// per 128 x 128 tile, several times the tile's MMA time at HBM bandwidth, so
+// their data path is what bounds them.  Three variants (template EXT):
+//   0  no bias, no emit;
+//   2  staged: the bias tile is cut into four 128 x 32 fp32 chunks (one
+//      128-byte swizzle atom wide) that warp 6 TMA-loads into a ring of
+//      shared-memory slots; each softmax thread reads its row of a chunk,
+//      writes the emitted logit back over the bias in place, and warp 7
+//      TMA-stores the chunk to the emit tensor before the slot is refilled.
+//      Needs 16-byte rows (N % 4 == 0) and 16-byte aligned bases;
+//   1  direct: per-thread global loads and stores of the row, for shapes
+//      the staged variant cannot map.
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -34,24 +49,36 @@ namespace {
 
 constexpr int kBlockM = 128;   // query rows per CTA
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy-rescale threshold in log2 units: the reference max is only raised when
 // a row's max grows by more than this (factor 2^8).
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kSmemBudget = 227 * 1024;
+constexpr int kResChunkCols = 32;                          // fp32 keys per chunk
+constexpr int kResChunks = kBlockN / kResChunkCols;        // chunks per key tile
+constexpr int kResChunkBytes = kBlockM * kResChunkCols * 4;
 
-template <int D>
+template <int EXT>
+constexpr int fwd_threads() { return EXT == 2 ? 256 : 192; }
+
+template <int D, int EXT>
 struct FwdCfg {
     static constexpr int kChunks = D / 64;              // 128-byte swizzle atoms per row
     static constexpr int kChunkBytes = kBlockM * 128;   // one atom column of a tile
     static constexpr int kTileBytes = kBlockM * D * 2;  // bf16 128 x D tile
-    static constexpr int kKStages = (D == 64) ? 3 : 2;
-    static constexpr int kVStages = (D == 64) ? 3 : 2;
+    // The staged residual variant is bound by its fp32 stream: it gives part
+    // of the K/V rings' shared memory to the residual slots (V_j is only
+    // needed a whole softmax after its load is issued, so one V stage holds).
+    static constexpr int kKStages = (D == 64) ? (EXT == 2 ? 2 : 3) : 2;
+    static constexpr int kVStages = (EXT == 2 ? (D == 64 ? 2 : 1) : kKStages);
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-    static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+    static constexpr int kOffRes = kOffV + kVStages * kTileBytes;
+    static constexpr int kResSlots =
+        EXT == 2 ? (kSmemBudget - 1024 - 512 - kOffRes) / kResChunkBytes : 0;
+    static constexpr int kOffBar = kOffRes + kResSlots * kResChunkBytes;
     // barrier indices
     static constexpr int kBarQFull = 0;
     static constexpr int kBarKFull = 1;
@@ -63,12 +90,16 @@ struct FwdCfg {
     static constexpr int kBarODone = kBarPFull + 2;
     static constexpr int kBarOFinal = kBarODone + 1;
     static constexpr int kBarDrain = kBarOFinal + 1;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarResFull = kBarDrain + 1;           // slot loaded (or granted)
+    static constexpr int kBarResDone = kBarResFull + kResSlots;  // softmax finished the slot
+    static constexpr int kBarResFree = kBarResDone + kResSlots;  // slot's store has read it
+    static constexpr int kNumBars = kBarResFree + kResSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem slot, abort flag
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+    static_assert(EXT != 2 || kResSlots >= kResChunks, "residual ring holds a key tile");
 };
 
 struct FwdParams {
@@ -79,7 +110,6 @@ struct FwdParams {
     int N, Hq, Hkv, group, BH, n_qtiles;
     float scale;        // scale of QK^T
     float scale_log2;   // scale * log2(e)
-    int vec4;           // bias/emit rows are 16-byte aligned (N % 4 == 0)
 };
 
 // Waits for the arrival of in-flight async work on the abort path only,
@@ -91,12 +121,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <int D, bool CAUSAL, bool EXT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, int EXT>
+__global__ void __launch_bounds__(fwd_threads<EXT>(), 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+           const __grid_constant__ CUtensorMap tmBias, const __grid_constant__ CUtensorMap tmEmit,
            const FwdParams p) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, EXT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -135,6 +166,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_init(bar(C::kBarODone), 1);
         mbar_init(bar(C::kBarOFinal), 1);
         mbar_init(bar(C::kBarDrain), 1);
+        for (int s = 0; s < C::kResSlots; ++s) {
+            mbar_init(bar(C::kBarResFull + s), 1);
+            mbar_init(bar(C::kBarResDone + s), kBlockM);
+            mbar_init(bar(C::kBarResFree + s), 1);
+        }
         fence_barrier_init();
     }
     if (warp == 5) {
@@ -146,6 +182,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmO);
+        if constexpr (EXT == 2) {
+            if (p.bias) tma_prefetch_desc(&tmBias);
+            if (p.emit) tma_prefetch_desc(&tmEmit);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -160,17 +200,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_3d(sb + C::kOffQ + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull), c * 64,
                             qt * kBlockM, bh);
+            // K runs one tile ahead of V: K_{j+1} only waits for S_{j+1-KStages}
+            // to finish with its stage, while V_j waits for PV_{j-VStages},
+            // which needs the softmax of that tile; issuing K first keeps the
+            // next S MMA from queueing behind a V wait.
             int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
+            auto load_k = [&](int j) -> bool {
                 const int ks = j % C::kKStages;
-                if (j >= C::kKStages)
-                    ok = mbar_wait(bar(C::kBarKEmpty + ks), ((j / C::kKStages) - 1) & 1, ac);
-                if (!ok) break;
+                if (j >= C::kKStages &&
+                    !mbar_wait(bar(C::kBarKEmpty + ks), ((j / C::kKStages) - 1) & 1, ac))
+                    return false;
                 mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &tmK,
                                 bar(C::kBarKFull + ks), c * 64, j * kBlockN, bh_kv);
                 k_issued = j + 1;
+                return true;
+            };
+            ok = load_k(0);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                if (j + 1 < n_kv) ok = load_k(j + 1);
+                if (!ok) break;
                 const int vs = j % C::kVStages;
                 if (j >= C::kVStages)
                     ok = mbar_wait(bar(C::kBarVEmpty + vs), ((j / C::kVStages) - 1) & 1, ac);
@@ -244,6 +294,83 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
         }
         __syncwarp();
+    } else if (EXT == 2 && warp == 6) {
+        // ------------------------------------------- residual chunk loader
+        // Chunk g = 4 j + c covers keys [128 j + 32 c, +32) of this query
+        // tile.  With a bias it is TMA-loaded (zero fill past N); without one
+        // the slot is only handed to the softmax, which writes the emitted
+        // logits into it.
+        if (lane == 0) {
+            const int n_chunks = n_kv * kResChunks;
+            bool ok = true;
+            int issued = 0;
+            int slot = 0;
+            uint32_t phase = 0;
+            for (int g = 0; g < n_chunks; ++g) {
+                if (g >= C::kResSlots) ok = mbar_wait(bar(C::kBarResFree + slot), phase ^ 1u, ac);
+                if (!ok) break;
+                const uint32_t full = bar(C::kBarResFull + slot);
+                if (p.bias) {
+                    mbar_arrive_expect_tx(full, kResChunkBytes);
+                    tma_load_3d(sb + C::kOffRes + slot * kResChunkBytes, &tmBias, full,
+                                (g / kResChunks) * kBlockN + (g % kResChunks) * kResChunkCols,
+                                qt * kBlockM, bh);
+                } else {
+                    mbar_arrive(full);
+                }
+                issued = g + 1;
+                if (++slot == C::kResSlots) { slot = 0; phase ^= 1u; }
+            }
+            if (!ok && p.bias) {
+                constexpr int kRing = C::kResSlots > 0 ? C::kResSlots : 1;
+                for (int g = max(issued - kRing, 0); g < issued; ++g)
+                    drain_wait(bar(C::kBarResFull + g % kRing),
+                               static_cast<uint32_t>(g / kRing) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (EXT == 2 && warp == 7) {
+        // ------------------------------------------- emitted-logit storer
+        // Waits until the softmax has written a chunk, TMA-stores it (clipped
+        // at N) and frees the slot once the store has read it.  While the
+        // next chunk is already done, one store is left reading so that two
+        // overlap.
+        if (lane == 0) {
+            const int n_chunks = n_kv * kResChunks;
+            int slot = 0;
+            uint32_t phase = 0;
+            int pending = -1;   // slot whose store may still be reading
+            for (int g = 0; g < n_chunks; ++g) {
+                if (!mbar_wait(bar(C::kBarResDone + slot), phase, ac)) break;
+                int nslot = slot + 1;
+                uint32_t nphase = phase;
+                if (nslot == C::kResSlots) { nslot = 0; nphase ^= 1u; }
+                if (p.emit) {
+                    tma_store_3d(&tmEmit, sb + C::kOffRes + slot * kResChunkBytes,
+                                 (g / kResChunks) * kBlockN + (g % kResChunks) * kResChunkCols,
+                                 qt * kBlockM, bh);
+                    tma_store_commit();
+                    const bool next_ready =
+                        g + 1 < n_chunks && mbar_test(bar(C::kBarResDone + nslot), nphase);
+                    if (next_ready) {
+                        tma_store_wait_read_n<1>();
+                        if (pending >= 0) mbar_arrive(bar(C::kBarResFree + pending));
+                        pending = slot;
+                    } else {
+                        tma_store_wait_read();
+                        if (pending >= 0) mbar_arrive(bar(C::kBarResFree + pending));
+                        mbar_arrive(bar(C::kBarResFree + slot));
+                        pending = -1;
+                    }
+                } else {
+                    mbar_arrive(bar(C::kBarResFree + slot));
+                }
+                slot = nslot;
+                phase = nphase;
+            }
+            tma_store_wait_read();
+        }
+        __syncwarp();
     } else {
         // ----------------------------------------------- softmax warpgroup
         const int r = threadIdx.x;             // row within the tile == TMEM lane
@@ -253,6 +380,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         float m_run = -INFINITY;   // running max, log2 units
         float l_run = 0.f;
         bool ok = true;
+        int res_slot = 0;          // residual ring position (staged variant)
+        uint32_t res_phase = 0;
 
         for (int j = 0; j < n_kv; ++j) {
             const int sbuf = j & 1;
@@ -270,48 +399,69 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const int key0 = j * kBlockN;
             const bool diag = CAUSAL && (j == qt);
             const bool ragged = key0 + kBlockN > p.N;
-            // x holds raw q.k when `raw` (scale > 0, no bias): the max commutes
-            // with the positive scale and the scale folds into the exp2 FMA.
-            // Otherwise x is turned into log2-unit logits t here.
-            bool raw = !EXT && p.scale_log2 > 0.f;
+            // x ends up holding values whose row max commutes with a positive
+            // factor `xmul` that turns them into log2-unit logits t; xmul then
+            // folds into the exp2 FMA.  No residual: x is raw q.k and xmul the
+            // scale (in log2 units) when that is positive, else x is turned
+            // into t here.  Residual: x is the natural-unit logit y and xmul
+            // log2(e).
+            float xmul = kLog2e;
 
-            if constexpr (EXT) {
+            if constexpr (EXT == 2) {
+                const uint64_t sc2 = f2pack(p.scale, p.scale);
+                // Natural-unit logit y = scale*qk + bias, chunk by chunk from
+                // the staged ring; y goes back over the bias for the storer
+                // (before the mask: masked entries of a diagonal tile are
+                // written too, which the emit contract leaves unspecified).
+                const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                for (int c = 0; c < kResChunks; ++c) {
+                    if (!mbar_wait_warp(bar(C::kBarResFull + res_slot), res_phase, ac)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t base = sb + C::kOffRes + res_slot * kResChunkBytes + row_off;
+#pragma unroll
+                    for (int k = 0; k < kResChunkCols / 4; ++k) {
+                        // 16-byte piece k of the row sits at k ^ (row % 8) (128-byte swizzle).
+                        const uint32_t addr = base + (static_cast<uint32_t>(k ^ (r & 7)) << 4);
+                        float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (p.bias) bv = ld_shared_f4(addr);
+                        const int col = c * kResChunkCols + k * 4;
+                        f2unpack(ffma2(f2pack(x[col], x[col + 1]), sc2, f2pack(bv.x, bv.y)),
+                                 x[col], x[col + 1]);
+                        f2unpack(ffma2(f2pack(x[col + 2], x[col + 3]), sc2, f2pack(bv.z, bv.w)),
+                                 x[col + 2], x[col + 3]);
+                        if (p.emit)
+                            st_shared_v4(addr, __float_as_uint(x[col]), __float_as_uint(x[col + 1]),
+                                         __float_as_uint(x[col + 2]),
+                                         __float_as_uint(x[col + 3]));
+                    }
+                    if (p.emit) fence_proxy_async_smem();
+                    mbar_arrive(bar(C::kBarResDone + res_slot));
+                    if (++res_slot == C::kResSlots) { res_slot = 0; res_phase ^= 1u; }
+                }
+                if (!ok) break;
+            } else if constexpr (EXT == 1) {
                 // Natural-unit logit = scale*qk + bias; emitted before the mask.
                 const size_t roff = (static_cast<size_t>(bh) * p.N + q_row) * p.N + key0;
                 const float *brow = (p.bias && row_valid) ? p.bias + roff : nullptr;
                 float *erow = (p.emit && row_valid) ? p.emit + roff : nullptr;
-                if (!diag && !ragged && p.vec4) {
+                const int lim = diag ? min(r + 1, kBlockN) : kBlockN;
 #pragma unroll
-                    for (int c = 0; c < kBlockN; c += 4) {
-                        float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (brow) bv = __ldg(reinterpret_cast<const float4 *>(brow + c));
-                        float4 y;
-                        y.x = fmaf(x[c + 0], p.scale, bv.x);
-                        y.y = fmaf(x[c + 1], p.scale, bv.y);
-                        y.z = fmaf(x[c + 2], p.scale, bv.z);
-                        y.w = fmaf(x[c + 3], p.scale, bv.w);
-                        if (erow) *reinterpret_cast<float4 *>(erow + c) = y;
-                        x[c + 0] = y.x * kLog2e;
-                        x[c + 1] = y.y * kLog2e;
-                        x[c + 2] = y.z * kLog2e;
-                        x[c + 3] = y.w * kLog2e;
-                    }
-                } else {
-                    const int lim = diag ? min(r + 1, kBlockN) : kBlockN;
-#pragma unroll
-                    for (int c = 0; c < kBlockN; ++c) {
-                        const bool inside = (c < lim) && (key0 + c < p.N);
-                        float bval = 0.f;
-                        if (brow && inside) bval = __ldg(brow + c);
-                        const float y = fmaf(x[c], p.scale, bval);
-                        if (erow && inside) erow[c] = y;
-                        x[c] = y * kLog2e;
-                    }
+                for (int c = 0; c < kBlockN; ++c) {
+                    const bool inside = (c < lim) && (key0 + c < p.N);
+                    float bval = 0.f;
+                    if (brow && inside) bval = __ldg(brow + c);
+                    x[c] = fmaf(x[c], p.scale, bval);
+                    if (erow && inside) erow[c] = x[c];
                 }
             } else {
-                if (!raw) {
+                xmul = p.scale_log2;
+                if (!(p.scale_log2 > 0.f)) {
 #pragma unroll
                     for (int c = 0; c < kBlockN; ++c) x[c] *= p.scale_log2;
+                    xmul = 1.f;
                 }
             }
 
@@ -334,7 +484,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             // (c runs 8, 24, ..., 120: elements 8..127 are all covered.)
             const float mt_x = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
                                      fmaxf(mx[6], mx[7]));
-            const float m_tile = raw ? mt_x * p.scale_log2 : mt_x;
+            const float m_tile = mt_x * xmul;
             // Lazy rescale: keep the previous reference max while the new row
             // max exceeds it by at most kRescaleLog2 (p stays <= 2^8); O/l and
             // LSE are unchanged by the choice of reference.
@@ -343,8 +493,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = ex2(m_run - m_use);   // 0 on the first tile
 
-            const float cmul = raw ? p.scale_log2 : 1.f;
-            const uint64_t cm2 = f2pack(cmul, cmul);
+            const uint64_t cm2 = f2pack(xmul, xmul);
             const uint64_t nm2 = f2pack(-m_use, -m_use);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // (+0.0f, +0.0f) pairs
             {
@@ -440,28 +589,35 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
 }
 
-template <int D, bool CAUSAL, bool EXT>
-cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     const CUtensorMap &to, const FwdParams &prm, unsigned grid,
-                     cudaStream_t stream) {
-    using C = FwdCfg<D>;
+struct FwdMaps {
+    CUtensorMap q, k, v, o, bias, emit;
+};
+
+template <int D, bool CAUSAL, int EXT>
+cudaError_t launch_t(const FwdMaps &m, const FwdParams &prm, unsigned grid, cudaStream_t stream) {
+    using C = FwdCfg<D, EXT>;
     auto kern = fwd_kernel<D, CAUSAL, EXT>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
+    kern<<<grid, fwd_threads<EXT>(), C::kSmemBytes, stream>>>(m.q, m.k, m.v, m.o, m.bias, m.emit,
+                                                               prm);
     return cudaGetLastError();
 }
 
+template <int D, bool CAUSAL>
+cudaError_t launch_c(int ext, const FwdMaps &m, const FwdParams &prm, unsigned grid,
+                     cudaStream_t stream) {
+    if (ext == 2) return launch_t<D, CAUSAL, 2>(m, prm, grid, stream);
+    if (ext == 1) return launch_t<D, CAUSAL, 1>(m, prm, grid, stream);
+    return launch_t<D, CAUSAL, 0>(m, prm, grid, stream);
+}
+
 template <int D>
-cudaError_t launch_d(bool causal, bool ext, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, const CUtensorMap &to, const FwdParams &prm,
-                     unsigned grid, cudaStream_t stream) {
-    if (causal)
-        return ext ? launch_t<D, true, true>(tq, tk, tv, to, prm, grid, stream)
-                   : launch_t<D, true, false>(tq, tk, tv, to, prm, grid, stream);
-    return ext ? launch_t<D, false, true>(tq, tk, tv, to, prm, grid, stream)
-               : launch_t<D, false, false>(tq, tk, tv, to, prm, grid, stream);
+cudaError_t launch_d(bool causal, int ext, const FwdMaps &m, const FwdParams &prm, unsigned grid,
+                     cudaStream_t stream) {
+    return causal ? launch_c<D, true>(ext, m, prm, grid, stream)
+                  : launch_c<D, false>(ext, m, prm, grid, stream);
 }
 
 }  // namespace
@@ -469,11 +625,11 @@ cudaError_t launch_d(bool causal, bool ext, const CUtensorMap &tq, const CUtenso
 cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     const long long BH = static_cast<long long>(pb.B) * pb.Hq;
     const long long BHkv = static_cast<long long>(pb.B) * pb.Hkv;
-    CUtensorMap tq, tk, tv, to;
-    if (!encode_bf16_rows(&tq, pb.q, pb.D, pb.N, BH, kBlockM) ||
-        !encode_bf16_rows(&tk, pb.k, pb.D, pb.N, BHkv, kBlockN) ||
-        !encode_bf16_rows(&tv, pb.v, pb.D, pb.N, BHkv, kBlockN) ||
-        !encode_bf16_rows(&to, pb.o, pb.D, pb.N, BH, kBlockM))
+    FwdMaps m;
+    if (!encode_bf16_rows(&m.q, pb.q, pb.D, pb.N, BH, kBlockM) ||
+        !encode_bf16_rows(&m.k, pb.k, pb.D, pb.N, BHkv, kBlockN) ||
+        !encode_bf16_rows(&m.v, pb.v, pb.D, pb.N, BHkv, kBlockN) ||
+        !encode_bf16_rows(&m.o, pb.o, pb.D, pb.N, BH, kBlockM))
         return cudaErrorInvalidValue;
     FwdParams prm;
     prm.bias = pb.bias;
@@ -488,13 +644,23 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     prm.n_qtiles = (pb.N + kBlockM - 1) / kBlockM;
     prm.scale = pb.scale;
     prm.scale_log2 = pb.scale * kLog2e;
-    prm.vec4 = (pb.N % 4 == 0) &&
-               (reinterpret_cast<uintptr_t>(pb.bias) % 16 == 0) &&
-               (reinterpret_cast<uintptr_t>(pb.emit) % 16 == 0);
     const unsigned grid = static_cast<unsigned>(prm.n_qtiles * BH);
-    const bool ext = (pb.bias != nullptr) || (pb.emit != nullptr);
-    if (pb.D == 64) return launch_d<64>(pb.causal, ext, tq, tk, tv, to, prm, grid, stream);
-    return launch_d<128>(pb.causal, ext, tq, tk, tv, to, prm, grid, stream);
+    int ext = 0;
+    if (pb.bias || pb.emit) {
+        // The staged variant maps the [N, N] planes as tensors of 128 x 32
+        // fp32 boxes: rows must be 16-byte multiples, bases 16-byte aligned.
+        const auto a16 = [](const void *ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+        ext = (pb.N % 4 == 0 && a16(pb.bias) && a16(pb.emit)) ? 2 : 1;
+        // A map of one operand stands in for the one that is absent (never used).
+        const float *rb = pb.bias ? pb.bias : pb.emit;
+        const float *re = pb.emit ? pb.emit : pb.bias;
+        if (ext == 2 && (!encode_f32_rows(&m.bias, rb, pb.N, pb.N, BH, kBlockM) ||
+                         !encode_f32_rows(&m.emit, re, pb.N, pb.N, BH, kBlockM)))
+            ext = 1;
+    }
+    if (ext != 2) m.bias = m.emit = m.q;   // unused by the kernel
+    if (pb.D == 64) return launch_d<64>(pb.causal, ext, m, prm, grid, stream);
+    return launch_d<128>(pb.causal, ext, m, prm, grid, stream);
 }
 
 }  // namespace tattn
