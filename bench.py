@@ -283,6 +283,12 @@ EXTRA_WORKLOADS = {
                            layers=4, B=1, Hq=20, Hkv=4, N=4096, D=128, causal=True),
     "tiny": dict(name="tiny_fwd_B1_H1_N128_D64", kind="fwd", B=1, Hq=1, Hkv=1, N=128, D=64,
                  causal=False),
+    # Smaller cases of the default step and of the residual chain for
+    # multi-pass ncu captures: inputs still larger than L2, well under 1 GB.
+    "profile_small": dict(name="causal_fwd_bwd_B1_H16_N8192_D128", B=1, Hq=16, Hkv=16, N=8192,
+                          D=128, causal=True),
+    "profile_chain_small": dict(name="residual_chain_4layers_B1_H8_KV2_N4096_D128", kind="chain",
+                                layers=4, B=1, Hq=8, Hkv=2, N=4096, D=128, causal=True),
 }
 
 
