@@ -19,24 +19,30 @@
 // Kernel").  exp is evaluated as 2^x with the scale folded in.
 //
 // Warp roles (one CTA per SM):
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r); also the
-//              O rescale and the epilogue.
-//   warp 4     TMA producer: Q once, then K_j / V_j through 1-3 stage rings.
-//   warp 5     TMEM allocator and single-thread tcgen05.mma issuer.
-//   warps 6-7  (staged residual only) fp32 bias loader and emitted-logit
+//   warps 0-7  two softmax warpgroups.  Thread r of warpgroup w owns query row
+//              r (TMEM lane r) for keys [64 w, 64 w + 64) of every key tile;
+//              the two swap partial row maxima through shared memory once per
+//              tile, so both scale by the same reference max.  Each rescales
+//              and stores its half of O's columns.
+//   warp 8     TMA producer: Q once, then K_j / V_j through 1-3 stage rings.
+//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer.
+//   warps 10-11  (staged residual only) fp32 bias loader and emitted-logit
 //              storer, see below.
 // TMEM (512 columns): S/P double buffer at columns 0 and 128, O at 256.
 // Issue order on the tensor core: S_0, S_1, PV_0, S_2, PV_1, ... so that the
-// softmax of tile j overlaps the MMAs of tiles j+1 and j-1.
+// softmax of tile j overlaps the MMAs of tiles j+1 and j-1.  Splitting a
+// tile's keys over two warpgroups halves the per-tile softmax latency (TMEM
+// load, 64 exp2 per thread instead of 128, P store), which is the critical
+// path of every tile.
 //
 // The residual variants (bias and/or emitted logits) move 2 x 64 KB of fp32
 // per 128 x 128 tile, several times the tile's MMA time at HBM bandwidth, so
 // their data path is what bounds them.  Three variants (template EXT):
 //   0  no bias, no emit;
 //   2  staged: the bias tile is cut into four 128 x 32 fp32 chunks (one
-//      128-byte swizzle atom wide) that warp 6 TMA-loads into a ring of
+//      128-byte swizzle atom wide) that warp 10 TMA-loads into a ring of
 //      shared-memory slots; each softmax thread reads its row of a chunk,
-//      writes the emitted logit back over the bias in place, and warp 7
+//      writes the emitted logit back over the bias in place, and warp 11
 //      TMA-stores the chunk to the emit tensor before the slot is refilled.
 //      Needs 16-byte rows (N % 4 == 0) and 16-byte aligned bases;
 //   1  direct: per-thread global loads and stores of the row, for shapes
@@ -59,8 +65,17 @@ constexpr int kResChunkCols = 32;                          // fp32 keys per chun
 constexpr int kResChunks = kBlockN / kResChunkCols;        // chunks per key tile
 constexpr int kResChunkBytes = kBlockM * kResChunkCols * 4;
 
+// Warp roles.  Warps 0-7 are two softmax warpgroups.
+constexpr int kSoftWarps = 8;
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kHalfN = kBlockN / 2;   // keys of a tile handled by one softmax warpgroup
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kWarpLoader = 10;       // staged residual only
+constexpr int kWarpStorer = 11;       // staged residual only
+
 template <int EXT>
-constexpr int fwd_threads() { return EXT == 2 ? 256 : 192; }
+constexpr int fwd_threads() { return EXT == 2 ? 384 : 320; }
 
 template <int D, int EXT>
 struct FwdCfg {
@@ -70,14 +85,16 @@ struct FwdCfg {
     // The staged residual variant is bound by its fp32 stream: it gives part
     // of the K/V rings' shared memory to the residual slots (V_j is only
     // needed a whole softmax after its load is issued, so one V stage holds).
-    static constexpr int kKStages = (D == 64) ? (EXT == 2 ? 2 : 3) : 2;
-    static constexpr int kVStages = (EXT == 2 ? (D == 64 ? 2 : 1) : kKStages);
+    static constexpr int kKStages = (D == 64) ? (EXT == 2 ? 2 : 3) : (EXT == 2 ? 1 : 2);
+    static constexpr int kVStages = kKStages;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kOffRes = kOffV + kVStages * kTileBytes;
+    static constexpr int kRedBytes = 2 * 2 * kBlockM * 4;   // row-max exchange, 2 buffers
     static constexpr int kResSlots =
-        EXT == 2 ? (kSmemBudget - 1024 - 512 - kOffRes) / kResChunkBytes : 0;
+        EXT == 2 ? (kSmemBudget - 512 - 16 - kRedBytes - kOffRes) / kResChunkBytes : 0;
+    static constexpr int kResRing = kResSlots > 0 ? kResSlots : 1;
     static constexpr int kOffBar = kOffRes + kResSlots * kResChunkBytes;
     // barrier indices
     static constexpr int kBarQFull = 0;
@@ -95,10 +112,13 @@ struct FwdCfg {
     static constexpr int kBarResFree = kBarResDone + kResSlots;  // slot's store has read it
     static constexpr int kNumBars = kBarResFree + kResSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem slot, abort flag
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
+    static constexpr int kOffRed = kOffMisc + 16;
+    static constexpr int kUsed = kOffRed + kRedBytes;
+    // Up to 1023 bytes of slack for aligning the base, as far as the budget allows.
+    static constexpr int kSmemBytes = kUsed + 1023 <= kSmemBudget ? kUsed + 1023 : kSmemBudget;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
-    static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+    static_assert(kUsed <= kSmemBudget, "shared memory budget");
     static_assert(EXT != 2 || kResSlots >= kResChunks, "residual ring holds a key tile");
 };
 
@@ -111,6 +131,18 @@ struct FwdParams {
     float scale;        // scale of QK^T
     float scale_log2;   // scale * log2(e)
 };
+
+// TMEM load / store of N consecutive 32-bit columns (N = 32 or 64).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 64) tmem_ld64(taddr, r);
+    else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 64) tmem_st64(taddr, r);
+    else tmem_st32(taddr, r);
+}
 
 // Waits for the arrival of in-flight async work on the abort path only,
 // ignoring the abort flag, with a short limit of its own.
@@ -131,6 +163,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // The layout needs a 1024-byte aligned base; refuse to run if the
+    // allocation cannot hold it after alignment.
+    if (smem - smem_raw + C::kUsed > C::kSmemBytes) {
+        if (threadIdx.x == 0) atomicCAS(p.status, kStatusOk, kStatusDeviceCheck);
+        return;
+    }
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -161,7 +199,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::kBarSFull + s), 1);
-            mbar_init(bar(C::kBarPFull + s), kBlockM);
+            mbar_init(bar(C::kBarPFull + s), kSoftThreads);
         }
         mbar_init(bar(C::kBarODone), 1);
         mbar_init(bar(C::kBarOFinal), 1);
@@ -173,11 +211,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kWarpProducer && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -192,7 +230,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kWarpProducer) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             bool ok = true;
@@ -242,7 +280,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
@@ -294,7 +332,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
         }
         __syncwarp();
-    } else if (EXT == 2 && warp == 6) {
+    } else if (EXT == 2 && warp == kWarpLoader) {
         // ------------------------------------------- residual chunk loader
         // Chunk g = 4 j + c covers keys [128 j + 32 c, +32) of this query
         // tile.  With a bias it is TMA-loaded (zero fill past N); without one
@@ -322,14 +360,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (++slot == C::kResSlots) { slot = 0; phase ^= 1u; }
             }
             if (!ok && p.bias) {
-                constexpr int kRing = C::kResSlots > 0 ? C::kResSlots : 1;
-                for (int g = max(issued - kRing, 0); g < issued; ++g)
-                    drain_wait(bar(C::kBarResFull + g % kRing),
-                               static_cast<uint32_t>(g / kRing) & 1u);
+                for (int g = max(issued - C::kResRing, 0); g < issued; ++g)
+                    drain_wait(bar(C::kBarResFull + g % C::kResRing),
+                               static_cast<uint32_t>(g / C::kResRing) & 1u);
             }
         }
         __syncwarp();
-    } else if (EXT == 2 && warp == 7) {
+    } else if (EXT == 2 && warp == kWarpStorer) {
         // ------------------------------------------- emitted-logit storer
         // Waits until the softmax has written a chunk, TMA-stores it (clipped
         // at N) and frees the slot once the store has read it.  While the
@@ -372,30 +409,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         __syncwarp();
     } else {
-        // ----------------------------------------------- softmax warpgroup
-        const int r = threadIdx.x;             // row within the tile == TMEM lane
-        const int q_row = qt * kBlockM + r;    // row within the head
+        // ---------------------------------------------- softmax warpgroups
+        // Warpgroup wg handles keys [64 wg, 64 wg + 64) of every key tile for
+        // all 128 rows; the two exchange their partial row max through shared
+        // memory once per tile, so they apply the same reference max, and each
+        // keeps its own partial row sum.  Every named barrier below is reached
+        // by all 256 threads the same number of times (failures are carried to
+        // the next barrier and leave through it together).
+        const int wg = warp >> 2;
+        const int r = ((warp & 3) << 5) | lane;   // row within the tile == TMEM lane
+        const int q_row = qt * kBlockM + r;       // row within the head
         const bool row_valid = q_row < p.N;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const int col0 = wg * kHalfN;             // first key of this warpgroup
+        float *red = reinterpret_cast<float *>(smem + C::kOffRed);   // [2][2][128]
         float m_run = -INFINITY;   // running max, log2 units
-        float l_run = 0.f;
+        float l_run = 0.f;         // this warpgroup's part of the row sum
         bool ok = true;
-        int res_slot = 0;          // residual ring position (staged variant)
-        uint32_t res_phase = 0;
 
         for (int j = 0; j < n_kv; ++j) {
             const int sbuf = j & 1;
-            ok = mbar_wait_warp(bar(C::kBarSFull + sbuf), (j >> 1) & 1, ac);
-            if (!ok) break;
-            tc_fence_after();
             const uint32_t tS = tmem + lane_base + sbuf * kBlockN;
-            float x[kBlockN];
-            {
-                uint32_t rr[kBlockN];
-                tmem_ld128(tS, rr);
-#pragma unroll
-                for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(rr[c]);
-            }
             const int key0 = j * kBlockN;
             const bool diag = CAUSAL && (j == qt);
             const bool ragged = key0 + kBlockN > p.N;
@@ -406,88 +440,118 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             // into t here.  Residual: x is the natural-unit logit y and xmul
             // log2(e).
             float xmul = kLog2e;
+            float x[kHalfN];
+            float mt_x = -INFINITY;
+            bool got = ok && mbar_wait_warp(bar(C::kBarSFull + sbuf), (j >> 1) & 1, ac);
+            if (got) {
+                tc_fence_after();
+                {
+                    uint32_t rr[kHalfN];
+                    tmem_ld64(tS + col0, rr);
+#pragma unroll
+                    for (int c = 0; c < kHalfN; ++c) x[c] = __uint_as_float(rr[c]);
+                }
 
-            if constexpr (EXT == 2) {
-                const uint64_t sc2 = f2pack(p.scale, p.scale);
-                // Natural-unit logit y = scale*qk + bias, chunk by chunk from
-                // the staged ring; y goes back over the bias for the storer
-                // (before the mask: masked entries of a diagonal tile are
-                // written too, which the emit contract leaves unspecified).
-                const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
+                if constexpr (EXT == 2) {
+                    const uint64_t sc2 = f2pack(p.scale, p.scale);
+                    // Natural-unit logit y = scale*qk + bias, chunk by chunk
+                    // from the staged ring; y goes back over the bias for the
+                    // storer (before the mask: masked entries of a diagonal
+                    // tile are written too, which the emit contract leaves
+                    // unspecified).
+                    const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-                for (int c = 0; c < kResChunks; ++c) {
-                    if (!mbar_wait_warp(bar(C::kBarResFull + res_slot), res_phase, ac)) {
-                        ok = false;
-                        break;
+                    for (int cc = 0; cc < kResChunks / 2; ++cc) {
+                        const int g = j * kResChunks + wg * (kResChunks / 2) + cc;
+                        const int slot = g % C::kResRing;
+                        const uint32_t phase = static_cast<uint32_t>(g / C::kResRing) & 1u;
+                        if (!mbar_wait_warp(bar(C::kBarResFull + slot), phase, ac)) {
+                            got = false;
+                            break;
+                        }
+                        const uint32_t base = sb + C::kOffRes + slot * kResChunkBytes + row_off;
+#pragma unroll
+                        for (int k = 0; k < kResChunkCols / 4; ++k) {
+                            // 16-byte piece k of the row sits at k ^ (row % 8)
+                            // (128-byte swizzle).
+                            const uint32_t addr = base + (static_cast<uint32_t>(k ^ (r & 7)) << 4);
+                            float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (p.bias) bv = ld_shared_f4(addr);
+                            const int col = cc * kResChunkCols + k * 4;
+                            f2unpack(ffma2(f2pack(x[col], x[col + 1]), sc2, f2pack(bv.x, bv.y)),
+                                     x[col], x[col + 1]);
+                            f2unpack(
+                                ffma2(f2pack(x[col + 2], x[col + 3]), sc2, f2pack(bv.z, bv.w)),
+                                x[col + 2], x[col + 3]);
+                            if (p.emit)
+                                st_shared_v4(addr, __float_as_uint(x[col]),
+                                             __float_as_uint(x[col + 1]),
+                                             __float_as_uint(x[col + 2]),
+                                             __float_as_uint(x[col + 3]));
+                        }
+                        if (p.emit) fence_proxy_async_smem();
+                        mbar_arrive(bar(C::kBarResDone + slot));
                     }
-                    const uint32_t base = sb + C::kOffRes + res_slot * kResChunkBytes + row_off;
+                } else if constexpr (EXT == 1) {
+                    // Natural-unit logit = scale*qk + bias; emitted before the mask.
+                    const size_t roff =
+                        (static_cast<size_t>(bh) * p.N + q_row) * p.N + key0 + col0;
+                    const float *brow = (p.bias && row_valid) ? p.bias + roff : nullptr;
+                    float *erow = (p.emit && row_valid) ? p.emit + roff : nullptr;
+                    const int lim = diag ? r + 1 - col0 : kHalfN;   // keys < lim are kept
 #pragma unroll
-                    for (int k = 0; k < kResChunkCols / 4; ++k) {
-                        // 16-byte piece k of the row sits at k ^ (row % 8) (128-byte swizzle).
-                        const uint32_t addr = base + (static_cast<uint32_t>(k ^ (r & 7)) << 4);
-                        float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (p.bias) bv = ld_shared_f4(addr);
-                        const int col = c * kResChunkCols + k * 4;
-                        f2unpack(ffma2(f2pack(x[col], x[col + 1]), sc2, f2pack(bv.x, bv.y)),
-                                 x[col], x[col + 1]);
-                        f2unpack(ffma2(f2pack(x[col + 2], x[col + 3]), sc2, f2pack(bv.z, bv.w)),
-                                 x[col + 2], x[col + 3]);
-                        if (p.emit)
-                            st_shared_v4(addr, __float_as_uint(x[col]), __float_as_uint(x[col + 1]),
-                                         __float_as_uint(x[col + 2]),
-                                         __float_as_uint(x[col + 3]));
+                    for (int c = 0; c < kHalfN; ++c) {
+                        const bool inside = (c < lim) && (key0 + col0 + c < p.N);
+                        float bval = 0.f;
+                        if (brow && inside) bval = __ldg(brow + c);
+                        x[c] = fmaf(x[c], p.scale, bval);
+                        if (erow && inside) erow[c] = x[c];
                     }
-                    if (p.emit) fence_proxy_async_smem();
-                    mbar_arrive(bar(C::kBarResDone + res_slot));
-                    if (++res_slot == C::kResSlots) { res_slot = 0; res_phase ^= 1u; }
-                }
-                if (!ok) break;
-            } else if constexpr (EXT == 1) {
-                // Natural-unit logit = scale*qk + bias; emitted before the mask.
-                const size_t roff = (static_cast<size_t>(bh) * p.N + q_row) * p.N + key0;
-                const float *brow = (p.bias && row_valid) ? p.bias + roff : nullptr;
-                float *erow = (p.emit && row_valid) ? p.emit + roff : nullptr;
-                const int lim = diag ? min(r + 1, kBlockN) : kBlockN;
+                } else {
+                    xmul = p.scale_log2;
+                    if (!(p.scale_log2 > 0.f)) {
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) {
-                    const bool inside = (c < lim) && (key0 + c < p.N);
-                    float bval = 0.f;
-                    if (brow && inside) bval = __ldg(brow + c);
-                    x[c] = fmaf(x[c], p.scale, bval);
-                    if (erow && inside) erow[c] = x[c];
+                        for (int c = 0; c < kHalfN; ++c) x[c] *= p.scale_log2;
+                        xmul = 1.f;
+                    }
                 }
-            } else {
-                xmul = p.scale_log2;
-                if (!(p.scale_log2 > 0.f)) {
-#pragma unroll
-                    for (int c = 0; c < kBlockN; ++c) x[c] *= p.scale_log2;
-                    xmul = 1.f;
-                }
-            }
 
-            if (diag || ragged) {
+                if (diag || ragged) {
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) {
-                    const bool keep = (!diag || c <= r) && (key0 + c < p.N);
-                    x[c] = keep ? x[c] : -INFINITY;
+                    for (int c = 0; c < kHalfN; ++c) {
+                        const int key = col0 + c;
+                        const bool keep = (!diag || key <= r) && (key0 + key < p.N);
+                        x[c] = keep ? x[c] : -INFINITY;
+                    }
                 }
+                // Partial row max as a tree (8 independent chains of 3-input max).
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+                for (int c = 8; c + 16 <= kHalfN; c += 16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 8 + i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], x[kHalfN - 8 + i]);
+                // (c runs 8, 24, 40 over elements 8..55; the last pass adds 56..63.)
+                mt_x = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
+                red[(sbuf * 2 + wg) * kBlockM + r] = mt_x;
+                tc_fence_before();   // this warpgroup's S reads precede the other's P writes
             }
-            // Row max as a tree (8 independent chains of 3-input max).
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = x[i];
-#pragma unroll
-            for (int c = 8; c < kBlockN; c += 16) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], x[c + i], x[c + 8 + i]);
+            if (named_bar_or(2, kSoftThreads, !got)) {
+                ok = false;
+                break;
             }
-            // (c runs 8, 24, ..., 120: elements 8..127 are all covered.)
-            const float mt_x = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                     fmaxf(mx[6], mx[7]));
-            const float m_tile = mt_x * xmul;
+            tc_fence_after();
+            const float mt_other = red[(sbuf * 2 + (wg ^ 1)) * kBlockM + r];
+            const float m_tile = fmaxf(mt_x, mt_other) * xmul;
             // Lazy rescale: keep the previous reference max while the new row
             // max exceeds it by at most kRescaleLog2 (p stays <= 2^8); O/l and
-            // LSE are unchanged by the choice of reference.
+            // LSE are unchanged by the choice of reference.  Both warpgroups
+            // compute the same m_new from the same inputs.
             float m_new = fmaxf(m_run, m_tile);
             if (m_new - m_run <= kRescaleLog2) m_new = m_run;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -497,16 +561,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const uint64_t nm2 = f2pack(-m_use, -m_use);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // (+0.0f, +0.0f) pairs
             {
-                uint32_t pk[kBlockN / 2];
+                uint32_t pk[kHalfN / 2];
 #pragma unroll
-                for (int c = 0; c < kBlockN / 2; ++c) {
+                for (int c = 0; c < kHalfN / 2; ++c) {
                     float t0, t1;
                     f2unpack(ffma2(f2pack(x[2 * c], x[2 * c + 1]), cm2, nm2), t0, t1);
                     const float p0 = ex2(t0), p1 = ex2(t1);
                     acc[c & 3] = fadd2(acc[c & 3], f2pack(p0, p1));
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                tmem_st64(tS, pk);
+                // P as packed bf16 pairs: keys 2c, 2c+1 of the tile in column c.
+                tmem_st32(tS + col0 / 2, pk);
             }
             float sum;
             {
@@ -519,61 +584,65 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
             const bool need = (j > 0) && (alpha < 1.f);
             if (__any_sync(0xffffffffu, need)) {
-                // O holds PV_0..PV_{j-1}; PV_{j-1} must have landed first.
-                ok = mbar_wait_warp(bar(C::kBarODone), (j - 1) & 1, ac);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t tO = tmem + lane_base + C::kColO;
-                const uint64_t a2 = f2pack(alpha, alpha);
+                // O holds PV_0..PV_{j-1}; PV_{j-1} must have landed first.  Each
+                // warpgroup rescales its half of O's columns.
+                if (!mbar_wait_warp(bar(C::kBarODone), (j - 1) & 1, ac)) {
+                    ok = false;   // leaves at the next barrier, with the other warpgroup
+                } else {
+                    tc_fence_after();
+                    const uint32_t tO = tmem + lane_base + C::kColO + wg * (D / 2);
+                    const uint64_t a2 = f2pack(alpha, alpha);
+                    uint32_t rr[D / 2];
+                    tmem_ld_cols<D / 2>(tO, rr);
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t rr[64];
-                    tmem_ld64(tO + c * 64, rr);
-#pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
+                    for (int e = 0; e < D / 2; e += 2) {
                         float o0 = __uint_as_float(rr[e]), o1 = __uint_as_float(rr[e + 1]);
                         f2unpack(fmul2(f2pack(o0, o1), a2), o0, o1);
                         rr[e] = __float_as_uint(o0);
                         rr[e + 1] = __float_as_uint(o1);
                     }
-                    tmem_st64(tO + c * 64, rr);
+                    tmem_st_cols<D / 2>(tO, rr);
                 }
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(C::kBarPFull + sbuf));
+            if (ok) mbar_arrive(bar(C::kBarPFull + sbuf));
             m_run = m_new;
         }
 
         // ------------------------------------------------------- epilogue
+        // Both warpgroups reach the barrier below exactly once, whatever
+        // happened in the loop.
         if (ok) ok = mbar_wait_warp(bar(C::kBarOFinal), 0, ac);
-        if (ok) {
+        float *lsum = red + (n_kv & 1) * 2 * kBlockM;   // buffer the last tile did not use
+        if (ok) lsum[wg * kBlockM + r] = l_run;
+        const bool fail = named_bar_or(2, kSoftThreads, !ok);
+        if (!fail) {
             tc_fence_after();
-            const float inv_l = 1.f / l_run;
-            const uint32_t tO = tmem + lane_base + C::kColO;
+            const float l_tot = l_run + lsum[(wg ^ 1) * kBlockM + r];
+            const float inv_l = 1.f / l_tot;
+            const uint32_t tO = tmem + lane_base + C::kColO + wg * (D / 2);
+            uint32_t rr[D / 2];
+            tmem_ld_cols<D / 2>(tO, rr);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t rr[64];
-                tmem_ld64(tO + c * 64, rr);
+            for (int pc = 0; pc < D / 16; ++pc) {   // 16-byte pieces of this half row
+                uint32_t w[4];
 #pragma unroll
-                for (int pc = 0; pc < 8; ++pc) {       // 16-byte pieces of this 64-column atom
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(rr[pc * 8 + 2 * e]) * inv_l,
-                                           __uint_as_float(rr[pc * 8 + 2 * e + 1]) * inv_l);
-                    const uint32_t addr = sb + C::kOffQ + c * C::kChunkBytes + r * 128 +
-                                          (static_cast<uint32_t>(pc ^ (r & 7)) << 4);
-                    st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-                }
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(rr[pc * 8 + 2 * e]) * inv_l,
+                                       __uint_as_float(rr[pc * 8 + 2 * e + 1]) * inv_l);
+                const int colg = wg * (D / 2) + pc * 8;   // first O column of the piece
+                const uint32_t addr = sb + C::kOffQ + (colg / 64) * C::kChunkBytes + r * 128 +
+                                      (static_cast<uint32_t>(((colg % 64) / 8) ^ (r & 7)) << 4);
+                st_shared_v4(addr, w[0], w[1], w[2], w[3]);
             }
-            if (p.lse && row_valid)
-                p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m_run + log2f(l_run)) * kLn2;
+            if (wg == 0 && p.lse && row_valid)
+                p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m_run + log2f(l_tot)) * kLn2;
             fence_proxy_async_smem();
         }
         tc_fence_before();
-        named_bar_sync(1, kBlockM);
-        if (threadIdx.x == 0 && *abort_flag == 0) {
+        named_bar_sync(1, kSoftThreads);
+        if (threadIdx.x == 0 && !fail && *abort_flag == 0) {
             for (int c = 0; c < C::kChunks; ++c)
                 tma_store_3d(&tmO, sb + C::kOffQ + c * C::kChunkBytes, c * 64, qt * kBlockM, bh);
             tma_store_commit();
@@ -583,7 +652,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
