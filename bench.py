@@ -283,6 +283,11 @@ EXTRA_WORKLOADS = {
                            layers=4, B=1, Hq=20, Hkv=4, N=4096, D=128, causal=True),
     "tiny": dict(name="tiny_fwd_B1_H1_N128_D64", kind="fwd", B=1, Hq=1, Hkv=1, N=128, D=64,
                  causal=False),
+    # Head dims 80 and 96 on the default step's shape (FLOPs at the true D).
+    "causal_fwd_bwd_d80": dict(name="causal_fwd_bwd_B1_H16_N16384_D80", B=1, Hq=16, Hkv=16,
+                               N=16384, D=80, causal=True),
+    "causal_fwd_bwd_d96": dict(name="causal_fwd_bwd_B1_H16_N16384_D96", B=1, Hq=16, Hkv=16,
+                               N=16384, D=96, causal=True),
     # Smaller cases of the default step and of the residual chain for
     # multi-pass ncu captures: inputs still larger than L2, well under 1 GB.
     "profile_small": dict(name="causal_fwd_bwd_B1_H16_N8192_D128", B=1, Hq=16, Hkv=16, N=8192,

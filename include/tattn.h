@@ -35,7 +35,7 @@
  *      bias, logits : fp32 [B, Hq,  N, N]
  *  - Grouped heads: query head h reads key/value head h / (Hq / Hkv);
  *    Hq must be a multiple of Hkv (Hkv == Hq is plain multi-head).
- *  - D must be 64 or 128.  N, B, Hq, Hkv are any positive sizes (N need not
+ *  - D must be 64, 80, 96 or 128.  N, B, Hq, Hkv are any positive sizes (N need not
  *    be a multiple of the 128-row tile); a zero size is an empty problem and
  *    returns ATTN_OK without launching anything.
  *  - Every tensor pointer is a DEVICE pointer of the current CUDA device,

@@ -59,7 +59,7 @@ def fwd(ta, **kw):
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1),
     (dict(q=A + 2), 1), (dict(k=A + 8), 1), (dict(o=A + 4), 1),
     (dict(bias=A + 2), 1), (dict(emit=A + 1), 1), (dict(lse=A + 3), 1),
-    (dict(D=96), 2), (dict(D=256), 2), (dict(D=0), 1), (dict(D=-64), 1),
+    (dict(D=72), 2), (dict(D=112), 2), (dict(D=256), 2), (dict(D=0), 1), (dict(D=-64), 1),
     (dict(Hkv=3), 1), (dict(Hkv=0), 1), (dict(B=-1), 1), (dict(N=-5), 1),
     (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
 ])
@@ -96,4 +96,7 @@ def test_workspace_size(ta):
     assert ta.attn_bwd_workspace_size(1, 1, 1, 5, 64) == 1280 + 2 * 512
     assert ta.attn_bwd_workspace_size(2, 3, 1, 130, 64) == (6 * 130 * 64 * 4 + 2 * 6 * 256 * 4)
     assert ta.attn_bwd_workspace_size(0, 1, 1, 3, 64) == 0
-    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 96) == 0
+    # D = 80 and 96 rows: 320- and 384-byte fp32 rows
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 80) == 1024 + 2 * 512
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 96) == 1280 + 2 * 512
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 112) == 0

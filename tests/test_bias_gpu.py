@@ -41,6 +41,8 @@ CASES = [
     (1, 2, 1, 260, 128, True),     # N % 32 != 0: ragged inside a staged fp32 chunk
     (1, 2, 2, 260, 128, False),
     (1, 2, 1, 640, 64, True),      # five key tiles: the staged ring wraps
+    (1, 2, 2, 256, 80, True),      # head dims 80 and 96
+    (1, 2, 1, 203, 96, False),
 ]
 
 

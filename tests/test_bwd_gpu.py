@@ -39,6 +39,8 @@ SHAPES = [
     (2, 2, 2, 129, 64),      # one row past a tile
     (1, 1, 1, 1, 128),       # single row
     (1, 6, 2, 256, 128),
+    (1, 2, 1, 384, 80),      # head dims 80 and 96: padded swizzle atoms, clipped stores
+    (1, 2, 2, 200, 96),      #   and a third fp32 dQ box clipped at D
 ]
 
 

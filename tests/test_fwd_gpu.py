@@ -58,6 +58,23 @@ SHAPES = [
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}H{s[1]}kv{s[2]}N{s[3]}" for s in SHAPES])
 def test_parity_small(ta, orc, D, causal, shape):
+    _parity(ta, orc, D, causal, shape)
+
+
+# Head dims 80 and 96: rows padded to two 128-byte swizzle atoms in shared
+# memory (zero-filled by TMA past D), stores clipped at D.
+SHAPES_ODD_D = [(1, 2, 2, 384), (1, 3, 1, 200), (2, 2, 1, 129), (1, 1, 1, 1)]
+
+
+@pytest.mark.parametrize("D", [80, 96])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES_ODD_D,
+                         ids=[f"B{s[0]}H{s[1]}kv{s[2]}N{s[3]}" for s in SHAPES_ODD_D])
+def test_parity_head_dim_80_96(ta, orc, D, causal, shape):
+    _parity(ta, orc, D, causal, shape)
+
+
+def _parity(ta, orc, D, causal, shape):
     B, Hq, Hkv, N = shape
     x = make_qkv(B, Hq, Hkv, N, D, seed=N + D)
     o, lse = run_fwd(ta, x, causal=causal)

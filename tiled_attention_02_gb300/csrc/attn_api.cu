@@ -42,7 +42,8 @@ attn_status check_sizes(int B, int Hq, int Hkv, int N, int D, float scale, bool 
     *empty = false;
     if (B < 0 || Hq < 0 || Hkv < 0 || N < 0) return ATTN_ERR_INVALID;
     if (!isfinite(scale)) return ATTN_ERR_INVALID;
-    if (D != 64 && D != 128) return (D > 0) ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID;
+    if (D != 64 && D != 80 && D != 96 && D != 128)
+        return (D > 0) ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID;
     if (B == 0 || Hq == 0 || N == 0) {
         *empty = true;
         return ATTN_OK;

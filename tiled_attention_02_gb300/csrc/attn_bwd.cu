@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(256)
 bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dO,
                const float *__restrict__ lse, float *__restrict__ lse2,
                float *__restrict__ delta, float *__restrict__ dq_acc, int N, int NP) {
-    constexpr int kLanesPerRow = D / 8;          // 8 bf16 (16 bytes) per lane
+    constexpr int kVecs = D / 8;                           // 16-byte vectors (8 bf16) per row
+    constexpr int kLanesPerRow = kVecs <= 8 ? 8 : 16;      // power of two >= kVecs
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
@@ -66,7 +67,7 @@ bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restr
         const bool valid = row < N;
         float acc = 0.f;
         const size_t off = (static_cast<size_t>(bh) * N + row) * D + sub * 8;
-        if (valid) {
+        if (valid && sub < kVecs) {
             const uint4 a = *reinterpret_cast<const uint4 *>(o + off);
             const uint4 b = *reinterpret_cast<const uint4 *>(dO + off);
             const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
@@ -116,9 +117,12 @@ constexpr int kMaxSmem = 232448;   // opt-in shared memory per block on sm_100/s
 
 template <int D>
 struct BwdCfg {
-    static constexpr int kChunks = D / 64;
+    // A bf16 row of D elements occupies ceil(D/64) 128-byte swizzle atoms
+    // (zero-filled past D by TMA); stores and reductions are clipped at D.
+    static constexpr int kChunks = (D + 63) / 64;
     static constexpr int kChunkBytes = kTile * 128;
-    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kDQBoxes = (D + 31) / 32;   // fp32 dQ boxes of 32 columns
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTileBytes;
     static constexpr int kOffStage = 2 * kTileBytes;          // 2 stages of {Q, dO}
@@ -144,7 +148,10 @@ struct BwdCfg {
     static constexpr int kUsed = kOffMisc + 16;
     static constexpr int kSmemBytes = (kUsed + 1023 <= kMaxSmem) ? kUsed + 1023 : kMaxSmem;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    // dK starts on a 64-column boundary so that 64-column loads stay aligned.
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
+    static constexpr uint32_t kColDK = D <= 64 ? 256 + 64 : 384;
+    static_assert(kDQBoxes * kTile * 128 <= 2 * kTileBytes, "dQ staging fits a stage");
     static_assert(kUsed <= kMaxSmem, "shared memory budget");
 };
 
@@ -372,12 +379,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after();
             const uint32_t stage = sb + C::kOffStage + s * C::kStageBytes;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < C::kDQBoxes; c += 2) {
+                // Two 32-column boxes per 64-column load; a last odd box
+                // (D = 80, 96) takes a 32-column load, whose columns past D
+                // are clipped by the reduction.
+                constexpr int kPair = 2;
                 uint32_t rr[64];
-                tmem_ld64(tDQ + c * 64, rr);
+                const int nb = (c + 1 < C::kDQBoxes) ? kPair : 1;
+                if (nb == 2) tmem_ld64(tDQ + c * 32, rr);
+                else tmem_ld32(tDQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {          // two 32-column boxes
-                    const uint32_t box = stage + (2 * c + hb) * (kTile * 128) + qr * 128;
+                for (int hb = 0; hb < kPair; ++hb) {
+                    if (hb >= nb) break;
+                    const uint32_t box = stage + (c + hb) * (kTile * 128) + qr * 128;
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
                         const int e = hb * 32 + ch * 4;
@@ -392,7 +406,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             named_bar_sync(2, kTile);
             if (qr == 0) {
                 const int qi = item_qi(j), bhq = item_bhq(j);
-                for (int bx = 0; bx < D / 32; ++bx)
+                for (int bx = 0; bx < C::kDQBoxes; ++bx)
                     tma_reduce_add_3d(&tmDQ, stage + bx * (kTile * 128), bx * 32, qi * kTile, bhq);
                 tma_store_commit();
                 tma_store_wait_read();
@@ -502,7 +516,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t col = w == 0 ? C::kColDV : C::kColDK;
             const uint32_t dst = w == 0 ? stV : stK;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < C::kChunks; ++c) {   // columns past D are clipped by the store
                 uint32_t rr[64];
                 tmem_ld64(tmem + lane_base + col + c * 64, rr);
                 uint32_t wv[32];
@@ -590,6 +604,8 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdProblem &pb, int *status, cudaStream_t stream) {
     if (pb.D == 64) return launch_d<64>(pb, status, stream);
+    if (pb.D == 80) return launch_d<80>(pb, status, stream);
+    if (pb.D == 96) return launch_d<96>(pb, status, stream);
     return launch_d<128>(pb, status, stream);
 }
 

@@ -79,9 +79,15 @@ constexpr int fwd_threads() { return EXT == 2 ? 384 : 320; }
 
 template <int D, int EXT>
 struct FwdCfg {
-    static constexpr int kChunks = D / 64;              // 128-byte swizzle atoms per row
-    static constexpr int kChunkBytes = kBlockM * 128;   // one atom column of a tile
-    static constexpr int kTileBytes = kBlockM * D * 2;  // bf16 128 x D tile
+    // A bf16 row of D elements occupies ceil(D/64) 128-byte swizzle atoms;
+    // for D = 80 or 96 the second atom is zero-filled past D by TMA, the MMAs
+    // use D/16 K-steps (QK^T) or N = D (PV), and stores are clipped at D.
+    static constexpr int kChunks = (D + 63) / 64;         // 128-byte swizzle atoms per row
+    static constexpr int kChunkBytes = kBlockM * 128;     // one atom column of a tile
+    static constexpr int kTileBytes = kChunks * kChunkBytes;   // bf16 128 x D tile, padded
+    // O columns [0, kOSplit) belong to softmax warpgroup 0, the rest to
+    // warpgroup 1 (each TMEM access stays aligned to its own width).
+    static constexpr int kOSplit = D > 64 ? 64 : D / 2;
     // The staged residual variant is bound by its fp32 stream: it gives part
     // of the K/V rings' shared memory to the residual slots (V_j is only
     // needed a whole softmax after its load is issued, so one V stage holds).
@@ -132,16 +138,40 @@ struct FwdParams {
     float scale_log2;   // scale * log2(e)
 };
 
-// TMEM load / store of N consecutive 32-bit columns (N = 32 or 64).
-template <int N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
-    if constexpr (N == 64) tmem_ld64(taddr, r);
-    else tmem_ld32(taddr, r);
+// O *= alpha on NC consecutive TMEM columns of this thread's row.
+template <int NC>
+__device__ __forceinline__ void o_rescale(uint32_t tO, float alpha) {
+    const uint64_t a2 = f2pack(alpha, alpha);
+    uint32_t rr[NC];
+    tmem_ld_cols<NC>(tO, rr);
+#pragma unroll
+    for (int e = 0; e < NC; e += 2) {
+        float o0 = __uint_as_float(rr[e]), o1 = __uint_as_float(rr[e + 1]);
+        f2unpack(fmul2(f2pack(o0, o1), a2), o0, o1);
+        rr[e] = __float_as_uint(o0);
+        rr[e + 1] = __float_as_uint(o1);
+    }
+    tmem_st_cols<NC>(tO, rr);
 }
-template <int N>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 64) tmem_st64(taddr, r);
-    else tmem_st32(taddr, r);
+
+// Row r's O columns [C0, C0 + NC), times 1/l, as bf16 into the 128-byte
+// swizzled output tile at `tile` (atoms of 64 columns, 128 rows each).
+template <int NC, int C0>
+__device__ __forceinline__ void o_stage(uint32_t tO, float inv_l, uint32_t tile, int r) {
+    uint32_t rr[NC];
+    tmem_ld_cols<NC>(tO, rr);
+#pragma unroll
+    for (int pc = 0; pc < NC / 8; ++pc) {   // 16-byte pieces
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(rr[pc * 8 + 2 * e]) * inv_l,
+                               __uint_as_float(rr[pc * 8 + 2 * e + 1]) * inv_l);
+        const int colg = C0 + pc * 8;   // first O column of the piece
+        const uint32_t addr = tile + (colg / 64) * (kBlockM * 128) + r * 128 +
+                              (static_cast<uint32_t>(((colg % 64) / 8) ^ (r & 7)) << 4);
+        st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+    }
 }
 
 // Waits for the arrival of in-flight async work on the abort path only,
@@ -590,18 +620,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     ok = false;   // leaves at the next barrier, with the other warpgroup
                 } else {
                     tc_fence_after();
-                    const uint32_t tO = tmem + lane_base + C::kColO + wg * (D / 2);
-                    const uint64_t a2 = f2pack(alpha, alpha);
-                    uint32_t rr[D / 2];
-                    tmem_ld_cols<D / 2>(tO, rr);
-#pragma unroll
-                    for (int e = 0; e < D / 2; e += 2) {
-                        float o0 = __uint_as_float(rr[e]), o1 = __uint_as_float(rr[e + 1]);
-                        f2unpack(fmul2(f2pack(o0, o1), a2), o0, o1);
-                        rr[e] = __float_as_uint(o0);
-                        rr[e + 1] = __float_as_uint(o1);
-                    }
-                    tmem_st_cols<D / 2>(tO, rr);
+                    const uint32_t tO = tmem + lane_base + C::kColO;
+                    if (wg == 0) o_rescale<C::kOSplit>(tO, alpha);
+                    else o_rescale<D - C::kOSplit>(tO + C::kOSplit, alpha);
                 }
             }
             tmem_st_wait();
@@ -621,21 +642,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tc_fence_after();
             const float l_tot = l_run + lsum[(wg ^ 1) * kBlockM + r];
             const float inv_l = 1.f / l_tot;
-            const uint32_t tO = tmem + lane_base + C::kColO + wg * (D / 2);
-            uint32_t rr[D / 2];
-            tmem_ld_cols<D / 2>(tO, rr);
-#pragma unroll
-            for (int pc = 0; pc < D / 16; ++pc) {   // 16-byte pieces of this half row
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(rr[pc * 8 + 2 * e]) * inv_l,
-                                       __uint_as_float(rr[pc * 8 + 2 * e + 1]) * inv_l);
-                const int colg = wg * (D / 2) + pc * 8;   // first O column of the piece
-                const uint32_t addr = sb + C::kOffQ + (colg / 64) * C::kChunkBytes + r * 128 +
-                                      (static_cast<uint32_t>(((colg % 64) / 8) ^ (r & 7)) << 4);
-                st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-            }
+            const uint32_t tO = tmem + lane_base + C::kColO;
+            if (wg == 0) o_stage<C::kOSplit, 0>(tO, inv_l, sb + C::kOffQ, r);
+            else o_stage<D - C::kOSplit, C::kOSplit>(tO + C::kOSplit, inv_l, sb + C::kOffQ, r);
             if (wg == 0 && p.lse && row_valid)
                 p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m_run + log2f(l_tot)) * kLn2;
             fence_proxy_async_smem();
@@ -728,8 +737,12 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
             ext = 1;
     }
     if (ext != 2) m.bias = m.emit = m.q;   // unused by the kernel
-    if (pb.D == 64) return launch_d<64>(pb.causal, ext, m, prm, grid, stream);
-    return launch_d<128>(pb.causal, ext, m, prm, grid, stream);
+    switch (pb.D) {
+    case 64: return launch_d<64>(pb.causal, ext, m, prm, grid, stream);
+    case 80: return launch_d<80>(pb.causal, ext, m, prm, grid, stream);
+    case 96: return launch_d<96>(pb.causal, ext, m, prm, grid, stream);
+    default: return launch_d<128>(pb.causal, ext, m, prm, grid, stream);
+    }
 }
 
 }  // namespace tattn

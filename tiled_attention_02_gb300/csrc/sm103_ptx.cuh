@@ -314,6 +314,39 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Loads 16 / 8 consecutive columns into r[] and waits for them.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TATTN_R8(0), TATTN_R8(8)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TATTN_R8(0)
+        : "r"(taddr)
+        : "memory");
+}
+// Stores r[] to 16 / 8 consecutive columns (wait with tmem_st_wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        TATTN_W8(0), TATTN_W8(8)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 TATTN_W8(0)
+                 : "memory");
+}
+
 // ---- generated wide TMEM accessors (one instruction per call) ----
 // Loads 64 consecutive columns into r[0..63] and waits for them.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
@@ -343,6 +376,41 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
 
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// N consecutive columns (N a multiple of 8, at most 128) through the widest
+// accessors that fit: r[0..N-1] <-> columns taddr .. taddr + N - 1.
+template <int N, int O = 0, int R>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[R]) {
+    static_assert(N % 8 == 0 && O + N <= R, "column count");
+    if constexpr (N >= 64) {
+        tmem_ld64(taddr, *reinterpret_cast<uint32_t(*)[64]>(&r[O]));
+        tmem_ld_cols<N - 64, O + 64>(taddr + 64, r);
+    } else if constexpr (N >= 32) {
+        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[O]));
+        tmem_ld_cols<N - 32, O + 32>(taddr + 32, r);
+    } else if constexpr (N >= 16) {
+        tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[O]));
+        tmem_ld_cols<N - 16, O + 16>(taddr + 16, r);
+    } else if constexpr (N >= 8) {
+        tmem_ld8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[O]));
+    }
+}
+template <int N, int O = 0, int R>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[R]) {
+    static_assert(N % 8 == 0 && O + N <= R, "column count");
+    if constexpr (N >= 64) {
+        tmem_st64(taddr, *reinterpret_cast<const uint32_t(*)[64]>(&r[O]));
+        tmem_st_cols<N - 64, O + 64>(taddr + 64, r);
+    } else if constexpr (N >= 32) {
+        tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&r[O]));
+        tmem_st_cols<N - 32, O + 32>(taddr + 32, r);
+    } else if constexpr (N >= 16) {
+        tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(&r[O]));
+        tmem_st_cols<N - 16, O + 16>(taddr + 16, r);
+    } else if constexpr (N >= 8) {
+        tmem_st8(taddr, *reinterpret_cast<const uint32_t(*)[8]>(&r[O]));
+    }
 }
 
 #undef TATTN_R8
