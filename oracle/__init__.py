@@ -68,14 +68,15 @@ def _load():
             lib.orc_set_threads.argtypes = [ctypes.c_int]
             lib.orc_get_threads.restype = ctypes.c_int
             lib.orc_fwd_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, _i64,
-                                         _dbl, ctypes.c_int, _ptr, _i64, ctypes.c_int, _ptr,
-                                         _ptr, _ptr]
+                                         _dbl, ctypes.c_int, _i64, _ptr, _i64, ctypes.c_int,
+                                         _ptr, _ptr, _ptr]
             lib.orc_delta_rows.argtypes = [_ptr, _ptr, _i64, _ptr, _i64, _ptr]
             lib.orc_bwd_dq_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
-                                            _i64, _i64, _dbl, ctypes.c_int, _ptr, _i64, _ptr]
+                                            _i64, _i64, _dbl, ctypes.c_int, _i64, _ptr, _i64,
+                                            _ptr]
             lib.orc_bwd_dkv_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
-                                             _i64, _i64, _dbl, ctypes.c_int, _ptr, _i64, _ptr,
-                                             _ptr]
+                                             _i64, _i64, _dbl, ctypes.c_int, _i64, _ptr, _i64,
+                                             _ptr, _ptr]
             _lib = lib
     return _lib
 
@@ -106,6 +107,16 @@ def _shapes(q, k, v):
     return B, Hq, Hkv, N, D
 
 
+def _window(causal, window) -> int:
+    """0 for no window; else the window length W >= 1 (causal only)."""
+    if window is None:
+        return 0
+    w = int(window)
+    if w < 1 or not causal:
+        raise ValueError("a sliding window needs causal=True and W >= 1")
+    return w
+
+
 def _rows(rows, total):
     if rows is None:
         return None, total
@@ -116,7 +127,7 @@ def _rows(rows, total):
 
 
 def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
-            emit_logits: bool = False, logits_out=None):
+            emit_logits: bool = False, logits_out=None, window=None):
     """Exact attention forward in fp64.
 
     q [B,Hq,N,D], k/v [B,Hkv,N,D] (any float dtype; widened to float64, which
@@ -124,16 +135,19 @@ def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
     bias [B,Hq,N,N] or None (widened to float64); with ``rows`` given, bias
     may instead be [nrows, N]: the bias rows of the requested rows only.
     rows: flat query-row indices ``(b*Hq + h)*N + i`` or None for all rows.
+    window: None, or W >= 1 with causal=True: key j is kept for query i iff
+    i - W < j <= i (sliding window over the W most recent keys).
 
     Returns dict with ``o`` ([B,Hq,N,D] when rows is None, else [nrows,D]),
     ``lse`` (matching) and, when ``emit_logits``, ``logits`` ([B,Hq,N,N] or
-    [nrows,N]) holding s_ij for kept keys and NaN where the causal mask hides
-    the key.  ``logits_out`` may be given (float64, right shape) to reuse a
+    [nrows,N]) holding s_ij for kept keys and NaN where the causal mask or
+    the window hides the key.  ``logits_out`` may be given (float64, right shape) to reuse a
     buffer; it may be the same array as ``bias`` when rows is None.
     """
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, N, D = _shapes(q, k, v)
+    w = _window(causal, window)
     total = B * Hq * N
     r, nrows = _rows(rows, total)
     if bias is not None:
@@ -159,7 +173,7 @@ def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
         else:
             logits = np.empty((nrows, N), dtype=np.float64)
     lib.orc_fwd_rows(_p(q), _p(k), _p(v), _p(bias), B, Hq, Hkv, N, D, float(scale),
-                     int(bool(causal)), _p(r), nrows, int(per_request), _p(o), _p(lse),
+                     int(bool(causal)), w, _p(r), nrows, int(per_request), _p(o), _p(lse),
                      _p(logits))
     out = {}
     if r is None:
@@ -169,14 +183,21 @@ def forward(q, k, v, *, scale: float, causal: bool, bias=None, rows=None,
         out["o"], out["lse"] = o, lse
     if emit_logits:
         if causal:
-            # Keys above the diagonal are not part of J_i: mark them NaN.
+            # Keys above the diagonal (and, with a window, keys j <= i - W)
+            # are not part of J_i: mark them NaN.
             if r is None:
                 iu = np.triu_indices(N, 1)
+                il = np.tril_indices(N, -w) if w else None
                 for lg in logits.reshape(B * Hq, N, N):
                     lg[iu] = np.nan
+                    if w:
+                        lg[il] = np.nan
             else:
                 lg = logits.reshape(nrows, N)
-                lg[np.arange(N)[None, :] > (r % N)[:, None]] = np.nan
+                jj, ii = np.arange(N)[None, :], (r % N)[:, None]
+                lg[jj > ii] = np.nan
+                if w:
+                    lg[jj <= ii - w] = np.nan
         out["logits"] = logits.reshape(B, Hq, N, N) if r is None else logits.reshape(nrows, N)
     return out
 
@@ -195,26 +216,27 @@ def delta(dO, o_rows, rows=None):
     return out
 
 
-def backward(q, k, v, dO, *, scale: float, causal: bool):
+def backward(q, k, v, dO, *, scale: float, causal: bool, window=None):
     """Exact dQ, dK, dV (fp64) for every row; returns dict with o, lse too."""
     lib = _load()
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     B, Hq, Hkv, N, D = _shapes(q, k, v)
-    fw = forward(q, k, v, scale=scale, causal=causal)
+    w = _window(causal, window)
+    fw = forward(q, k, v, scale=scale, causal=causal, window=window)
     lse = np.ascontiguousarray(fw["lse"].reshape(-1))
     dlt = delta(dO, fw["o"].reshape(-1, D))
     dq = np.empty((B * Hq * N, D), dtype=np.float64)
     dk = np.empty((B * Hkv * N, D), dtype=np.float64)
     dv = np.empty((B * Hkv * N, D), dtype=np.float64)
     lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                        float(scale), int(bool(causal)), None, B * Hq * N, _p(dq))
+                        float(scale), int(bool(causal)), w, None, B * Hq * N, _p(dq))
     lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                         float(scale), int(bool(causal)), None, B * Hkv * N, _p(dk), _p(dv))
+                         float(scale), int(bool(causal)), w, None, B * Hkv * N, _p(dk), _p(dv))
     return {"o": fw["o"], "lse": fw["lse"], "dq": dq.reshape(B, Hq, N, D),
             "dk": dk.reshape(B, Hkv, N, D), "dv": dv.reshape(B, Hkv, N, D)}
 
 
-def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows):
+def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows, window=None):
     """dQ at flat query rows ``q_rows`` and dK/dV at flat key rows ``k_rows``.
 
     Key row flat index is ``(b*Hkv + g)*N + j``.  The statistics LSE and Delta
@@ -225,27 +247,31 @@ def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows)
     lib = _load()
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     B, Hq, Hkv, N, D = _shapes(q, k, v)
+    w = _window(causal, window)
     group = Hq // Hkv
     qr, nq = _rows(q_rows, B * Hq * N)
     kr, nk = _rows(k_rows, B * Hkv * N)
     # Query rows whose statistics are needed.
     need = set() if qr is None else {int(x) for x in qr}
     # A key row j of kv head (b, g) needs every query row of the group's
-    # heads that attends to it: i >= j under the causal mask, all i otherwise.
-    first = {}
+    # heads that attends to it: j <= i < j + W under the causal mask (W = N
+    # without a window), all i otherwise.
+    spans = {}
     for x in (kr if kr is not None else []):
         bg, j = divmod(int(x), N)
         b, g = divmod(bg, Hkv)
         lo = j if causal else 0
+        hi = min(N, j + w) if w else N
         for h in range(g * group, (g + 1) * group):
-            first[b * Hq + h] = min(first.get(b * Hq + h, N), lo)
-    for bh, lo in first.items():
-        need |= set(range(bh * N + lo, bh * N + N))
+            spans.setdefault(b * Hq + h, []).append((lo, hi))
+    for bh, sp in spans.items():
+        for lo, hi in sp:
+            need |= set(range(bh * N + lo, bh * N + hi))
     stat_rows = np.asarray(sorted(need), dtype=np.int64)
     lse = np.zeros((B * Hq * N,), dtype=np.float64)
     dlt = np.zeros((B * Hq * N,), dtype=np.float64)
     if stat_rows.size:
-        fw = forward(q, k, v, scale=scale, causal=causal, rows=stat_rows)
+        fw = forward(q, k, v, scale=scale, causal=causal, rows=stat_rows, window=window)
         lse[stat_rows] = fw["lse"]
         dlt[stat_rows] = delta(dO, fw["o"], stat_rows)
     dq = np.empty((nq, D), dtype=np.float64)
@@ -253,8 +279,8 @@ def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows)
     dv = np.empty((nk, D), dtype=np.float64)
     if nq:
         lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                            float(scale), int(bool(causal)), _p(qr), nq, _p(dq))
+                            float(scale), int(bool(causal)), w, _p(qr), nq, _p(dq))
     if nk:
         lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                             float(scale), int(bool(causal)), _p(kr), nk, _p(dk), _p(dv))
+                             float(scale), int(bool(causal)), w, _p(kr), nk, _p(dk), _p(dv))
     return {"dq": dq, "dk": dk, "dv": dv}

@@ -12,7 +12,9 @@
  *   kv head      g   = h / (Hq / Hkv)   (contiguous groups of query heads
  *                                        share one key/value head)
  *   key set      J_i = {0..N-1}, or {0..i} when causal (key j is kept
- *                      for query i iff j <= i, diagonal included)
+ *                      for query i iff j <= i, diagonal included); with a
+ *                      sliding window of W keys, J_i = {max(0, i-W+1)..i}
+ *                      (key j kept iff i - W < j <= i)
  *   logit        s_ij = scale * sum_d q[i,d] k[j,d]  (+ bias[i,j])
  *   row max      m_i  = max_{j in J_i} s_ij
  *   row sum      l_i  = sum_{j in J_i} exp(s_ij - m_i)
@@ -29,6 +31,11 @@
  *    causal mask hides the strict upper triangle (triu, diagonal = 1).
  *  - blog.ans20xx.com/posts/ai/day26, "最小 attention wrapper": the naive
  *    attention with a lower-triangular (tril) keep mask and scale d^-0.5.
+ *  - Sliding-window (local) attention: "FlashAttention原理与Triton实战",
+ *    sections 3.1 and 7 (a window mask stacked on the causal kernel) and the
+ *    Block Attention Residual page, "实验结果" (an SWA baseline).  The pages
+ *    give no formula; the window here is the causal one over the W most
+ *    recent keys, the query's own key included.
  *  - Block Attention Residual Triton kernel (iqiancheng.github.io), section
  *    "Block Attention Residual 做了什么": softmax(Q_i K_i^T / sqrt(d) +
  *    logit_residual_{i-1}); the residual is added unscaled to the scaled
@@ -79,10 +86,11 @@ int orc_get_threads(void)
 #endif
 }
 
-/* Number of keys a query row attends to: |J_i|. */
-static int64_t key_count(int64_t i, int64_t N, int causal)
+/* J_i as the half-open key range [*j0, *j1); window <= 0 means none. */
+static void key_range(int64_t i, int64_t N, int causal, int64_t window, int64_t *j0, int64_t *j1)
 {
-    return causal ? i + 1 : N;
+    *j1 = causal ? i + 1 : N;
+    *j0 = (causal && window > 0 && i - window + 1 > 0) ? i - window + 1 : 0;
 }
 
 /* s_ij for every j in J_i of one query row, written to s[0..|J_i|). */
@@ -124,8 +132,8 @@ static void row_stats(const double *s, int64_t nk, double *m_out, double *l_out)
  */
 void orc_fwd_rows(const double *q, const double *k, const double *v, const double *bias,
                   int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t D,
-                  double scale, int causal, const int64_t *rows, int64_t nrows,
-                  int bias_per_request, double *o, double *lse, double *logits)
+                  double scale, int causal, int64_t window, const int64_t *rows,
+                  int64_t nrows, int bias_per_request, double *o, double *lse, double *logits)
 {
     (void)B;
     const int64_t group = Hq / Hkv;
@@ -143,23 +151,25 @@ void orc_fwd_rows(const double *q, const double *k, const double *v, const doubl
             const double *k_head = k + (b * Hkv + g) * N * D;
             const double *v_head = v + (b * Hkv + g) * N * D;
             const double *bias_row = bias ? bias + (bias_per_request ? r : flat) * N : NULL;
-            const int64_t nk = key_count(i, N, causal);
+            int64_t j0, j1;
+            key_range(i, N, causal, window, &j0, &j1);
+            const int64_t nk = j1 - j0;   /* s[t] is the logit of key j0 + t */
 
-            row_logits(q_row, k_head, bias_row, nk, D, scale, s);
+            row_logits(q_row, k_head + j0 * D, bias_row ? bias_row + j0 : NULL, nk, D, scale, s);
             double m, l;
             row_stats(s, nk, &m, &l);
 
             double *o_row = o + r * D;
             for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;
-            for (int64_t j = 0; j < nk; ++j) {
-                const double p = exp(s[j] - m) / l;
+            for (int64_t t = 0; t < nk; ++t) {
+                const double p = exp(s[t] - m) / l;
                 for (int64_t d = 0; d < D; ++d)
-                    o_row[d] += p * v_head[j * D + d];
+                    o_row[d] += p * v_head[(j0 + t) * D + d];
             }
             if (lse) lse[r] = m + log(l);
             if (logits) {
                 double *out = logits + r * N;
-                for (int64_t j = 0; j < nk; ++j) out[j] = s[j];
+                for (int64_t t = 0; t < nk; ++t) out[j0 + t] = s[t];
             }
         }
         free(s);
@@ -191,8 +201,8 @@ void orc_delta_rows(const double *dO, const double *o, int64_t D,
 void orc_bwd_dq_rows(const double *q, const double *k, const double *v, const double *dO,
                      const double *lse, const double *delta,
                      int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t D,
-                     double scale, int causal, const int64_t *rows, int64_t nrows,
-                     double *dq)
+                     double scale, int causal, int64_t window, const int64_t *rows,
+                     int64_t nrows, double *dq)
 {
     (void)B;
     const int64_t group = Hq / Hkv;
@@ -209,13 +219,16 @@ void orc_bwd_dq_rows(const double *q, const double *k, const double *v, const do
             const double *k_head = k + (b * Hkv + g) * N * D;
             const double *v_head = v + (b * Hkv + g) * N * D;
             const double *do_row = dO + flat * D;
-            const int64_t nk = key_count(i, N, causal);
+            int64_t j0, j1;
+            key_range(i, N, causal, window, &j0, &j1);
+            const int64_t nk = j1 - j0;
 
-            row_logits(q + flat * D, k_head, NULL, nk, D, scale, s);
+            row_logits(q + flat * D, k_head + j0 * D, NULL, nk, D, scale, s);
             double *dq_row = dq + r * D;
             for (int64_t d = 0; d < D; ++d) dq_row[d] = 0.0;
-            for (int64_t j = 0; j < nk; ++j) {
-                const double p = exp(s[j] - lse[flat]);
+            for (int64_t t = 0; t < nk; ++t) {
+                const int64_t j = j0 + t;
+                const double p = exp(s[t] - lse[flat]);
                 double dp = 0.0;
                 for (int64_t d = 0; d < D; ++d)
                     dp += do_row[d] * v_head[j * D + d];
@@ -237,8 +250,8 @@ void orc_bwd_dq_rows(const double *q, const double *k, const double *v, const do
 void orc_bwd_dkv_rows(const double *q, const double *k, const double *v, const double *dO,
                       const double *lse, const double *delta,
                       int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t D,
-                      double scale, int causal, const int64_t *krows, int64_t nkrows,
-                      double *dk, double *dv)
+                      double scale, int causal, int64_t window, const int64_t *krows,
+                      int64_t nkrows, double *dk, double *dv)
 {
     (void)B;
     const int64_t group = Hq / Hkv;
@@ -255,8 +268,10 @@ void orc_bwd_dkv_rows(const double *q, const double *k, const double *v, const d
         for (int64_t d = 0; d < D; ++d) { dk_row[d] = 0.0; dv_row[d] = 0.0; }
 
         for (int64_t h = g * group; h < (g + 1) * group; ++h) {
-            const int64_t i0 = causal ? j : 0;   /* j in J_i  <=>  i >= j when causal */
-            for (int64_t i = i0; i < N; ++i) {
+            /* j in J_i  <=>  j <= i (causal) and i < j + W (window) */
+            const int64_t i0 = causal ? j : 0;
+            const int64_t i1 = (causal && window > 0 && j + window < N) ? j + window : N;
+            for (int64_t i = i0; i < i1; ++i) {
                 const int64_t qflat = (b * Hq + h) * N + i;
                 const double *q_row = q + qflat * D;
                 const double *do_row = dO + qflat * D;

@@ -19,11 +19,16 @@ MUTANTS = [
     ("bias_wrong_row", "bias + (bias_per_request ? r : flat) * N", "bias + (bias_per_request ? r : flat) * N + 1"),
     ("bias_scaled", "s[j] = scale * dot + (bias_row ? bias_row[j] : 0.0);",
      "s[j] = scale * (dot + (bias_row ? bias_row[j] : 0.0));"),
-    ("causal_excludes_diagonal", "return causal ? i + 1 : N;", "return causal ? i : N;"),
-    ("causal_one_extra_key", "return causal ? i + 1 : N;", "return causal ? (i + 2 < N ? i + 2 : N) : N;"),
+    ("causal_excludes_diagonal", "*j1 = causal ? i + 1 : N;", "*j1 = causal ? i : N;"),
+    ("causal_one_extra_key", "*j1 = causal ? i + 1 : N;", "*j1 = causal ? (i + 2 < N ? i + 2 : N) : N;"),
+    ("window_one_extra_key", "i - window + 1 > 0) ? i - window + 1 : 0;",
+     "i - window > 0) ? i - window : 0;"),
+    ("window_ignored", "*j0 = (causal && window > 0", "*j0 = (causal && window > 1000000"),
+    ("dkv_window_one_extra_query", "(causal && window > 0 && j + window < N) ? j + window : N;",
+     "(causal && window > 0 && j + window + 1 < N) ? j + window + 1 : N;"),
     ("gqa_modulo_mapping", "const int64_t g = h / group;\n            const double *q_row",
      "const int64_t g = h % Hkv;\n            const double *q_row"),
-    ("no_max_subtraction", "const double p = exp(s[j] - m) / l;", "const double p = exp(s[j]) / l;"),
+    ("no_max_subtraction", "const double p = exp(s[t] - m) / l;", "const double p = exp(s[t]) / l;"),
     ("lse_base2", "if (lse) lse[r] = m + log(l);", "if (lse) lse[r] = m + log2(l);"),
     ("lse_missing_max", "if (lse) lse[r] = m + log(l);", "if (lse) lse[r] = log(l);"),
     ("ds_sign_dq", "const double ds = p * (dp - delta[flat]);", "const double ds = p * (delta[flat] - dp);"),

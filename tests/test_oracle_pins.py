@@ -395,3 +395,112 @@ def test_per_request_bias_rows_equal_full_bias(orc):
         np.testing.assert_array_equal(p["o"], f["o"].reshape(-1, D)[rows])
         np.testing.assert_array_equal(p["logits"], f["logits"].reshape(-1, N)[rows])
         full_bias = f["logits"]
+
+
+# ------------------------------------------------------- sliding window
+# Reading of the pages: [FA-Triton] 3.1 / 7 name a window mask stacked on the
+# causal kernel and [BlockRes] "实验结果" an SWA baseline, with no formula; the
+# window is taken as the W most recent keys, the query's own included:
+# key j is kept for query i iff i - W < j <= i.
+
+def test_window_one_keeps_only_the_diagonal(orc):
+    """W = 1: each query sees only its own key, so P_ii = 1, O_i = v_i and
+    LSE_i = s_ii = scale q_i . k_i exactly."""
+    B, Hq, Hkv, N, D = 1, 4, 2, 6, 3
+    q, k, v = rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D)
+    out = orc.forward(q, k, v, scale=0.7, causal=True, window=1)
+    for h in range(Hq):
+        g = h // 2
+        np.testing.assert_array_equal(out["o"][0, h], v[0, g])
+        np.testing.assert_allclose(out["lse"][0, h], 0.7 * (q[0, h] * k[0, g]).sum(-1),
+                                   rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("W", [2, 3, 5])
+def test_window_zero_query_gives_mean_of_last_w_values(orc, W):
+    """Q = 0: uniform weights over the last min(i+1, W) keys, so O_i is the
+    mean of v[max(0, i-W+1) .. i] and LSE_i = ln min(i+1, W)."""
+    B, H, N, D = 1, 2, 8, 4
+    q = np.zeros((B, H, N, D))
+    k, v = rand(B, H, N, D), rand(B, H, N, D)
+    out = orc.forward(q, k, v, scale=0.9, causal=True, window=W)
+    for h in range(H):
+        for i in range(N):
+            lo = max(0, i - W + 1)
+            np.testing.assert_allclose(out["o"][0, h, i], v[0, h, lo:i + 1].mean(axis=0),
+                                       rtol=0, atol=1e-14)
+            assert abs(out["lse"][0, h, i] - math.log(i + 1 - lo)) < 1e-14
+
+
+def test_window_at_least_n_equals_causal(orc):
+    B, Hq, Hkv, N, D = 1, 2, 1, 7, 3
+    q, k, v = rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D)
+    bias = rand(B, Hq, N, N)
+    c = orc.forward(q, k, v, scale=0.5, causal=True, bias=bias, emit_logits=True)
+    for W in (N, N + 5):
+        w = orc.forward(q, k, v, scale=0.5, causal=True, bias=bias, emit_logits=True, window=W)
+        np.testing.assert_array_equal(w["o"], c["o"])
+        np.testing.assert_array_equal(w["lse"], c["lse"])
+        np.testing.assert_array_equal(w["logits"], c["logits"])
+
+
+def test_window_matches_library_softmax_on_tiny_inputs(orc):
+    """Brute force: an explicit band mask (numpy tril minus tril(-W)) applied
+    to the full logit matrix, scipy-style softmax, matmul with V."""
+    B, Hq, Hkv, N, D, W = 2, 4, 2, 9, 5, 3
+    q, k, v = rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D)
+    bias = rand(B, Hq, N, N)
+    kr, vr = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    band = np.tril(np.ones((N, N), dtype=bool)) & ~np.tril(np.ones((N, N), dtype=bool), -W)
+    s = 0.35 * np.matmul(q, np.swapaxes(kr, -1, -2)) + bias
+    want = np.matmul(softmax_rows(np.where(band, s, -np.inf)), vr)
+    out = orc.forward(q, k, v, scale=0.35, causal=True, bias=bias, window=W, emit_logits=True)
+    np.testing.assert_allclose(out["o"], want, rtol=0, atol=1e-13)
+    lg = out["logits"]
+    assert np.isnan(lg[..., ~band]).all()
+    np.testing.assert_allclose(lg[..., band], s[..., band], rtol=0, atol=1e-13)
+
+
+def test_window_backward_matches_finite_differences(orc):
+    B, Hq, Hkv, N, D, W = 1, 2, 1, 6, 3, 2
+    scale = 0.6
+    q, k, v, do = rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D), rand(B, Hq, N, D)
+    g = orc.backward(q, k, v, do, scale=scale, causal=True, window=W)
+
+    def L(qq, kk, vv):
+        return float((orc.forward(qq, kk, vv, scale=scale, causal=True, window=W)["o"] * do).sum())
+
+    h = 1e-5
+    for name, arr in (("dq", q), ("dk", k), ("dv", v)):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            args = {"q": q, "k": k, "v": v}
+            a = arr.copy(); a[idx] += h
+            b = arr.copy(); b[idx] -= h
+            args[name[1]] = a
+            lp = L(args["q"], args["k"], args["v"])
+            args[name[1]] = b
+            lm = L(args["q"], args["k"], args["v"])
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.abs(g[name] - fd).max() / max(1.0, np.abs(fd).max())
+        assert err < 1e-7, (name, err)
+
+
+def test_window_backward_sampled_equals_full(orc):
+    B, Hq, Hkv, N, D, W = 1, 4, 2, 10, 3, 3
+    q, k, v, do = rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D), rand(B, Hq, N, D)
+    full = orc.backward(q, k, v, do, scale=0.5, causal=True, window=W)
+    qr, kr = np.array([0, 3, 12, 39]), np.array([0, 4, 9, 13, 19])
+    part = orc.backward_sampled(q, k, v, do, scale=0.5, causal=True, q_rows=qr, k_rows=kr,
+                                window=W)
+    np.testing.assert_allclose(part["dq"], full["dq"].reshape(-1, D)[qr], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(part["dk"], full["dk"].reshape(-1, D)[kr], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(part["dv"], full["dv"].reshape(-1, D)[kr], rtol=0, atol=1e-14)
+
+
+def test_window_needs_causal(orc):
+    x = rand(1, 1, 4, 2)
+    with pytest.raises(ValueError):
+        orc.forward(x, x, x, scale=1.0, causal=False, window=2)
+    with pytest.raises(ValueError):
+        orc.forward(x, x, x, scale=1.0, causal=True, window=0)
