@@ -41,15 +41,29 @@ WORKLOAD = dict(name="causal_fwd_bwd_B1_H16_N16384_D128", B=1, Hq=16, Hkv=16, N=
 L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2
 
 
-def attn_flops(B, H, N, D, causal):
+def attn_flops(B, H, N, D, causal, window=None):
     """Forward FLOPs by the pages' count 4*B*H*N^2*D (blog.ans20xx.com day26,
-    'CUDA event 计时模板'), halved for the causal mask."""
+    'CUDA event 计时模板'), halved for the causal mask.  A causal sliding
+    window of W < N keys counts N*W - W^2/2 (query, key) pairs per head, the
+    same continuous count that gives N^2/2 at W = N."""
+    if causal and window and window < N:
+        return 4.0 * B * H * D * (N * window - window * window / 2)
     f = 4.0 * B * H * N * N * D
     return f / 2 if causal else f
 
 
-def bwd_flops(B, H, N, D, causal):
-    return 2.5 * attn_flops(B, H, N, D, causal)
+def bwd_flops(B, H, N, D, causal, window=None):
+    return 2.5 * attn_flops(B, H, N, D, causal, window)
+
+
+def tile_pairs(B, H, N, causal, window=None):
+    """(128-row query tile, 128-key tile) pairs the kernels process."""
+    n_qt = (N + 127) // 128
+    if not causal:
+        return B * H * n_qt * n_qt
+    if not window or window >= N:
+        return B * H * n_qt * (n_qt + 1) // 2
+    return B * H * sum(qt - max(0, qt * 128 - window + 1) // 128 + 1 for qt in range(n_qt))
 
 
 def peaks():
@@ -270,6 +284,8 @@ def config_block(world, W=None):
            "l2": "flushed between timed steps (256 MB write)"}
     if W.get("kind") == "chain":
         cfg["layers"] = W["layers"]
+    if W.get("window"):
+        cfg["window"] = W["window"]
     return cfg
 
 
@@ -288,6 +304,9 @@ EXTRA_WORKLOADS = {
                                N=16384, D=80, causal=True),
     "causal_fwd_bwd_d96": dict(name="causal_fwd_bwd_B1_H16_N16384_D96", B=1, Hq=16, Hkv=16,
                                N=16384, D=96, causal=True),
+    # Causal sliding window of 4096 keys on the default step's shape.
+    "swa_fwd_bwd": dict(name="swa4096_fwd_bwd_B1_H16_N16384_D128", B=1, Hq=16, Hkv=16, N=16384,
+                        D=128, causal=True, window=4096),
     # Smaller cases of the default step and of the residual chain for
     # multi-pass ncu captures: inputs still larger than L2, well under 1 GB.
     "profile_small": dict(name="causal_fwd_bwd_B1_H16_N8192_D128", B=1, Hq=16, Hkv=16, N=8192,
@@ -357,12 +376,20 @@ def run_ours(args):
         o = torch.empty_like(q)
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
 
+        window = W.get("window")
+
         def fwd():
-            s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, o.data_ptr(),
-                                lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal, None, sh)
+            if window:
+                s = ta.raw_attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
+                                           o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                           window, None, sh)
+            else:
+                s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
+                                    o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                    causal, None, sh)
             assert s == 0, s
         io_bytes = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-        phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal), io_bytes))
+        phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal, window), io_bytes))
         host_inputs += [x["q"], x["k"], x["v"]]
         dev_inputs += [q, k, v]
         results = [o]
@@ -373,13 +400,20 @@ def run_ours(args):
                              dtype=torch.uint8, device=dev)
 
             def bwd():
-                s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                    lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                    dv.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
-                                    ws.data_ptr(), ws.numel(), sh)
+                if window:
+                    s = ta.raw_attn_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B,
+                                               Hq, Hkv, N, D, scale, window, ws.data_ptr(),
+                                               ws.numel(), sh)
+                else:
+                    s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                        dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                        causal, ws.data_ptr(), ws.numel(), sh)
                 assert s == 0, s
             bwd_bytes = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-            phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal), bwd_bytes))
+            phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal, window), bwd_bytes))
             host_inputs.append(x["do"])
             dev_inputs.append(do)
             results = [dq, dk, dv]
@@ -462,9 +496,9 @@ def run_ours(args):
     # The dominant kernel by device time decides the roofline entry; every
     # phase is reported under "kernels".
     pk = peaks()
-    n_qt = (N + 127) // 128
-    units = B * Hq * (n_qt * (n_qt + 1) // 2 if causal else n_qt * n_qt)   # 128x128 tile pairs
-    tag = f"{'causal' if causal else 'noncausal'}_B{B}_H{Hq}_N{N}_D{D}"
+    units = tile_pairs(B, Hq, N, causal, W.get("window"))   # 128x128 tile pairs
+    tag = (f"{'causal' if causal else 'noncausal'}_B{B}_H{Hq}_N{N}_D{D}"
+           + (f"_W{W['window']}" if W.get("window") else ""))
     kernels = {}
     for (lbl, _, fl, by), avg in zip(phases, ph_avg):
         if kind == "chain":

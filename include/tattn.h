@@ -19,6 +19,7 @@
  *    and the tiled double loop: kwkr.cn/news/592482, 2.2 and 2.3.
  *  - Causal mask (key j kept for query i iff j <= i): kwkr.cn/news/592482,
  *    3.3 and 3.4; blog.ans20xx.com/posts/ai/day26, "最小 attention wrapper".
+ *  - Sliding-window mask: see attn_fwd_window.
  *  - Additive pre-softmax logit bias read from the previous layer and the
  *    logits emitted for the next layer (block attention residual):
  *    Block Attention Residual Triton kernel (iqiancheng.github.io), sections
@@ -109,6 +110,28 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, const float *b
                      float *emit_logits, void *stream);
 
 /*
+ * Forward pass with a causal sliding window.
+ *
+ * The pages name a window mask stacked on the causal kernel
+ * ("FlashAttention原理与Triton实战", sections 3.1 and 7) and a sliding-window
+ * (SWA) baseline model (Block Attention Residual page, "实验结果"), without a
+ * formula.  Here, key j is kept for query i iff  i - window < j <= i : the
+ * `window` most recent keys, the query's own included.  window >= N is the
+ * plain causal mask.
+ *
+ * Arguments, layouts, ownership and errors are those of attn_fwd with
+ * causal = 1, plus:
+ *   window       sliding-window length W >= 1 (ATTN_ERR_INVALID otherwise).
+ * Only the 128 x 128 key tiles that hold a kept key are read (bias) or
+ * written (emit_logits); masked entries inside those tiles hold
+ * unspecified emitted values.
+ */
+attn_status attn_fwd_window(const void *q, const void *k, const void *v, const float *bias,
+                            void *o, float *lse,
+                            int B, int Hq, int Hkv, int N, int D, float scale, int window,
+                            float *emit_logits, void *stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,Hq,N,D], plus two fp32 per-row arrays [B*Hq, NP]
  * (NP = N rounded up to a multiple of 128) holding LSE*log2(e) and
@@ -141,6 +164,17 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      void *dq, void *dk, void *dv,
                      int B, int Hq, int Hkv, int N, int D, float scale, int causal,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass of attn_fwd_window (same q, k, v, scale and window; no bias).
+ * Arguments, workspace, layouts and errors are those of attn_bwd with
+ * causal = 1, plus window >= 1 as in attn_fwd_window.
+ */
+attn_status attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, const void *dO,
+                            void *dq, void *dk, void *dv,
+                            int B, int Hq, int Hkv, int N, int D, float scale, int window,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Size of the fixed device scratch behind attn_bwd_noalloc: 32 MiB.  A shape

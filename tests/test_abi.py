@@ -100,3 +100,21 @@ def test_workspace_size(ta):
     assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 80) == 1024 + 2 * 512
     assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 96) == 1280 + 2 * 512
     assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 112) == 0
+
+
+@pytest.mark.parametrize("window", [0, -1, -128])
+def test_window_entry_points_reject_bad_window(ta, window):
+    """window must be >= 1; rejected on the host before anything runs."""
+    assert ta.raw_attn_fwd_window(A, A, A, None, A, A, 1, 2, 2, 256, 64, 0.125, window, None,
+                                  None) == 1
+    assert ta.raw_attn_bwd_window(A, A, A, A, A, A, A, A, A, 1, 2, 2, 256, 64, 0.125, window, A,
+                                  1 << 30, None) == 1
+
+
+def test_window_entry_points_check_shapes_like_the_plain_ones(ta):
+    assert ta.raw_attn_fwd_window(A, A, A, None, A, A, 1, 2, 2, 256, 72, 0.125, 64, None,
+                                  None) == 2
+    assert ta.raw_attn_fwd_window(A, A, A, None, A, A, 1, 2, 2, 0, 64, 0.125, 64, None,
+                                  None) == 0
+    assert ta.raw_attn_bwd_window(A + 2, A, A, A, A, A, A, A, A, 1, 2, 2, 256, 64, 0.125, 64, A,
+                                  1 << 30, None) == 1

@@ -55,3 +55,15 @@ def test_chain_bytes(bench):
     io = bench.chain_layer_bytes(W, 0) - kept
     assert [bench.chain_layer_bytes(W, i) - io for i in range(4)] == [kept, 2 * kept, 2 * kept, kept]
     assert 6 * kept / 1e9 == pytest.approx(4.03, rel=0.01)
+
+
+def test_window_counts_reduce_to_causal():
+    """A window of at least N keys is the causal mask: same FLOPs, same tile
+    pairs; W = 128 on two tiles touches (0,0), (1,0), (1,1)."""
+    import bench
+    assert bench.attn_flops(1, 2, 1024, 64, True, 1024) == bench.attn_flops(1, 2, 1024, 64, True)
+    assert bench.tile_pairs(1, 2, 1024, True, 4096) == bench.tile_pairs(1, 2, 1024, True)
+    assert bench.tile_pairs(1, 1, 256, True, 128) == 3
+    assert bench.tile_pairs(1, 1, 256, True, 1) == 2
+    # W keys per row once i >= W: N*W - W^2/2 pairs in the continuous count
+    assert bench.attn_flops(1, 1, 1000, 1, True, 100) == 4.0 * (1000 * 100 - 100 * 100 / 2)

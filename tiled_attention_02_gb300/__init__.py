@@ -32,8 +32,9 @@ ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_DEVICE_CHECK = 5
 
 # Every symbol include/tattn.h declares.
-EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_noalloc",
-            "attn_status_string", "attn_last_device_status", "attn_version")
+EXPORTED = ("attn_fwd", "attn_fwd_window", "attn_bwd_workspace_size", "attn_bwd",
+            "attn_bwd_window", "attn_bwd_noalloc", "attn_status_string",
+            "attn_last_device_status", "attn_version")
 
 # Size of the fixed device scratch attn_bwd_noalloc uses (include/tattn.h).
 ATTN_BWD_NOALLOC_SCRATCH_BYTES = 33554432
@@ -66,11 +67,16 @@ def lib() -> ctypes.CDLL:
             vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]
             L.attn_fwd.restype = i
+            L.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]
+            L.attn_fwd_window.restype = i
             L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
             L.attn_bwd_workspace_size.restype = sz
             L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
                                    sz, vp]
             L.attn_bwd.restype = i
+            L.attn_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                          i, vp, sz, vp]
+            L.attn_bwd_window.restype = i
             L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                            f, i, vp]
             L.attn_bwd_noalloc.restype = i
@@ -121,20 +127,34 @@ def raw_attn_fwd(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, scale, causal, emit, s
                           int(causal), emit, stream)
 
 
+def raw_attn_fwd_window(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, scale, window, emit,
+                       stream) -> int:
+    return lib().attn_fwd_window(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, ctypes.c_float(scale),
+                                 int(window), emit, stream)
+
+
 def raw_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal, ws,
                  ws_bytes, stream) -> int:
     return lib().attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D,
                           ctypes.c_float(scale), int(causal), ws, ws_bytes, stream)
 
 
+def raw_attn_bwd_window(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D, scale, window, ws,
+                        ws_bytes, stream) -> int:
+    return lib().attn_bwd_window(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D,
+                                 ctypes.c_float(scale), int(window), ws, ws_bytes, stream)
+
+
 def attn_fwd(q, k, v, bias=None, *, scale: float | None = None, causal: bool = False,
-             o=None, lse=None, emit_logits=None, want_lse: bool = True, stream=None):
+             o=None, lse=None, emit_logits=None, want_lse: bool = True, stream=None,
+             window: int | None = None):
     """Exact attention forward through the C ABI.
 
     q [B,Hq,N,D], k/v [B,Hkv,N,D] bf16 CUDA tensors; bias (optional) fp32
     [B,Hq,N,N]; emit_logits (optional) fp32 [B,Hq,N,N] output buffer, which
-    may be ``bias`` itself.  Returns ``(o, lse)`` (lse is None when
-    ``want_lse`` is False and no ``lse`` buffer is given).
+    may be ``bias`` itself.  ``window`` (with causal=True): causal sliding
+    window of that many keys (attn_fwd_window).  Returns ``(o, lse)`` (lse
+    is None when ``want_lse`` is False and no ``lse`` buffer is given).
     """
     import torch
     B, Hq, N, D = q.shape
@@ -152,8 +172,15 @@ def attn_fwd(q, k, v, bias=None, *, scale: float | None = None, causal: bool = F
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
     _check(lse, "lse", torch.float32, (B, Hq, N))
-    st = raw_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(lse), B, Hq, Hkv, N,
-                      D, scale, causal, _ptr(emit_logits), _stream_handle(stream))
+    if window is not None:
+        if not causal:
+            raise ValueError("a sliding window needs causal=True")
+        st = raw_attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(lse), B,
+                                 Hq, Hkv, N, D, scale, window, _ptr(emit_logits),
+                                 _stream_handle(stream))
+    else:
+        st = raw_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                          N, D, scale, causal, _ptr(emit_logits), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
     return o, lse
@@ -164,7 +191,8 @@ def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, D: int) -> int:
 
 
 def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = False,
-             dq=None, dk=None, dv=None, workspace=None, stream=None):
+             dq=None, dk=None, dv=None, workspace=None, stream=None,
+             window: int | None = None):
     """Backward by recomputation through the C ABI; returns (dq, dk, dv)."""
     import torch
     B, Hq, N, D = q.shape
@@ -184,9 +212,17 @@ def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = 
     need = attn_bwd_workspace_size(B, Hq, Hkv, N, D)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = raw_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
-                      _ptr(dk), _ptr(dv), B, Hq, Hkv, N, D, scale, causal, _ptr(workspace),
-                      workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if window is not None:
+        if not causal:
+            raise ValueError("a sliding window needs causal=True")
+        st = raw_attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, D, scale, window,
+                                 _ptr(workspace), ws_bytes, _stream_handle(stream))
+    else:
+        st = raw_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                          _ptr(dk), _ptr(dv), B, Hq, Hkv, N, D, scale, causal, _ptr(workspace),
+                          ws_bytes, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv

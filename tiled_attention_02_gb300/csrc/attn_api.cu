@@ -117,11 +117,12 @@ int *device_status_ptr() {
 
 using namespace tattn;
 
-extern "C" {
+namespace {
 
-attn_status attn_fwd(const void *q, const void *k, const void *v, const float *bias, void *o,
+// window: 0 for none, else W >= 1 (checked by the caller; implies causal).
+attn_status fwd_impl(const void *q, const void *k, const void *v, const float *bias, void *o,
                      float *lse, int B, int Hq, int Hkv, int N, int D, float scale, int causal,
-                     float *emit_logits, void *stream) {
+                     int window, float *emit_logits, void *stream) {
     bool empty = false;
     attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
     if (st != ATTN_OK || empty) return st;
@@ -151,6 +152,7 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, const float *b
     pb.D = D;
     pb.scale = scale;
     pb.causal = causal != 0;
+    pb.window = (window > 0 && window < N) ? window : 0;   // W >= N is the causal mask
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
     cudaError_t e = launch_fwd(pb, status, static_cast<cudaStream_t>(stream));
@@ -158,16 +160,11 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, const float *b
 }
 
 
-size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D) {
-    bool empty = false;
-    if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
-    return bwd_workspace_layout(B, Hq, N, D).total;
-}
 
-attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const float *lse,
                      const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N,
-                     int D, float scale, int causal, void *workspace, size_t workspace_bytes,
-                     void *stream) {
+                     int D, float scale, int causal, int window, void *workspace,
+                     size_t workspace_bytes, void *stream) {
     bool empty = false;
     attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
     if (st != ATTN_OK || empty) return st;
@@ -196,6 +193,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
     pb.D = D;
     pb.scale = scale;
     pb.causal = causal != 0;
+    pb.window = (window > 0 && window < N) ? window : 0;
     char *ws = static_cast<char *>(workspace);
     pb.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
     pb.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
@@ -206,6 +204,48 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
     cudaError_t e = launch_bwd(pb, status, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D) {
+    bool empty = false;
+    if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
+    return bwd_workspace_layout(B, Hq, N, D).total;
+}
+
+attn_status attn_fwd(const void *q, const void *k, const void *v, const float *bias, void *o,
+                     float *lse, int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                     float *emit_logits, void *stream) {
+    return fwd_impl(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, scale, causal, 0, emit_logits,
+                    stream);
+}
+
+attn_status attn_fwd_window(const void *q, const void *k, const void *v, const float *bias,
+                            void *o, float *lse, int B, int Hq, int Hkv, int N, int D,
+                            float scale, int window, float *emit_logits, void *stream) {
+    if (window < 1) return ATTN_ERR_INVALID;
+    return fwd_impl(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, scale, 1, window, emit_logits,
+                    stream);
+}
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N,
+                     int D, float scale, int causal, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal, 0,
+                    workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                            int B, int Hq, int Hkv, int N, int D, float scale, int window,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    if (window < 1) return ATTN_ERR_INVALID;
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, D, scale, 1, window,
+                    workspace, workspace_bytes, stream);
 }
 
 const char *attn_status_string(attn_status s) {

@@ -162,6 +162,7 @@ struct BwdParams {
     int *status;
     int N, NP, Hq, Hkv, group, BHkv, n_tiles;
     float scale, scale_log2;
+    int window;   // causal sliding window W (key j kept for query i iff i - W < j), 0 = none
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -216,8 +217,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int kt = blockIdx.x / p.BHkv;
     const int bh_kv = blockIdx.x % p.BHkv;
     const int b = bh_kv / p.Hkv, g = bh_kv % p.Hkv;
+    // Query tiles q_lo .. q_lo + nq - 1 see this key tile: from the diagonal
+    // (causal) to the tile holding query kt*128 + 127 + W - 1 (window).
     const int q_lo = CAUSAL ? kt : 0;
-    const int nq = p.n_tiles - q_lo;              // query tiles per query head
+    const int q_end = (CAUSAL && p.window > 0)
+                          ? min(p.n_tiles, (kt * kTile + kTile - 1 + p.window - 1) / kTile + 1)
+                          : p.n_tiles;
+    const int nq = q_end - q_lo;                  // query tiles per query head
     const int n_items = p.group * nq;
 
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
@@ -436,6 +442,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && (item_qi(j) == kt);
+            // Some query column of the tile lies W or more rows past some key row.
+            const int qoff = (item_qi(j) - kt) * kTile;   // query row - key row offset of the tiles
+            const bool wedge = CAUSAL && p.window > 0 && qoff + kTile - 1 >= p.window;
             const uint32_t s_lse = s_rows + s * kTile * 4 + w * 256;
             const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4 + w * 256;
             uint32_t pw[32];   // P^T of this warpgroup's 64 columns, bf16 pairs
@@ -452,10 +461,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         f2unpack(ffma2(f2pack(__uint_as_float(sr[c + u]), __uint_as_float(sr[c + u + 1])),
                                        sc2, f2pack(-la, -lb)), t0, t1);
                         float p0 = ex2(t0), p1 = ex2(t1);
-                        if (diag) {
-                            const int q = w * 64 + c + u;
-                            p0 = (kr <= q) ? p0 : 0.f;
-                            p1 = (kr <= q + 1) ? p1 : 0.f;
+                        if (diag || wedge) {
+                            // kept iff 0 <= query - key < W (no upper limit without a window)
+                            const int dq0 = qoff + w * 64 + c + u - kr;
+                            const int wl = wedge ? p.window : (1 << 30);
+                            p0 = (dq0 >= 0 && dq0 < wl) ? p0 : 0.f;
+                            p1 = (dq0 + 1 >= 0 && dq0 + 1 < wl) ? p1 : 0.f;
                         }
                         pw[(c + u) >> 1] = pack_bf16x2(p0, p1);
                     }
@@ -585,6 +596,7 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     prm.n_tiles = n_tiles;
     prm.scale = pb.scale;
     prm.scale_log2 = pb.scale * kLog2e;
+    prm.window = pb.causal ? pb.window : 0;
     const unsigned grid = static_cast<unsigned>(n_tiles * BHkv);
     auto kern = pb.causal ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);

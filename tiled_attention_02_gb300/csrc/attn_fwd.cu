@@ -136,6 +136,7 @@ struct FwdParams {
     int N, Hq, Hkv, group, BH, n_qtiles;
     float scale;        // scale of QK^T
     float scale_log2;   // scale * log2(e)
+    int window;         // causal sliding window W (key j kept iff i - W < j), 0 = none
 };
 
 // O *= alpha on NC consecutive TMEM columns of this thread's row.
@@ -209,7 +210,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int bh = blk % p.BH;
     const int bh_kv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
     const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
-    const int n_kv = CAUSAL ? min(qt + 1, n_ktiles) : n_ktiles;
+    // Key tiles kv_lo .. kv_lo + n_kv - 1: the causal mask ends them at the
+    // diagonal tile, a sliding window starts them at the tile holding key
+    // row_lo - W + 1 (the first key the tile's first row keeps).
+    const int row_lo = qt * kBlockM;
+    const int kv_lo = (CAUSAL && p.window > 0) ? max(0, row_lo - p.window + 1) / kBlockN : 0;
+    const int n_kv = (CAUSAL ? min(qt + 1, n_ktiles) : n_ktiles) - kv_lo;
 
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -281,7 +287,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &tmK,
-                                bar(C::kBarKFull + ks), c * 64, j * kBlockN, bh_kv);
+                                bar(C::kBarKFull + ks), c * 64, (kv_lo + j) * kBlockN, bh_kv);
                 k_issued = j + 1;
                 return true;
             };
@@ -296,7 +302,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &tmV,
-                                bar(C::kBarVFull + vs), c * 64, j * kBlockN, bh_kv);
+                                bar(C::kBarVFull + vs), c * 64, (kv_lo + j) * kBlockN, bh_kv);
                 v_issued = j + 1;
             }
             if (!ok) {
@@ -381,7 +387,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (p.bias) {
                     mbar_arrive_expect_tx(full, kResChunkBytes);
                     tma_load_3d(sb + C::kOffRes + slot * kResChunkBytes, &tmBias, full,
-                                (g / kResChunks) * kBlockN + (g % kResChunks) * kResChunkCols,
+                                (kv_lo + g / kResChunks) * kBlockN +
+                                    (g % kResChunks) * kResChunkCols,
                                 qt * kBlockM, bh);
                 } else {
                     mbar_arrive(full);
@@ -414,7 +421,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (nslot == C::kResSlots) { nslot = 0; nphase ^= 1u; }
                 if (p.emit) {
                     tma_store_3d(&tmEmit, sb + C::kOffRes + slot * kResChunkBytes,
-                                 (g / kResChunks) * kBlockN + (g % kResChunks) * kResChunkCols,
+                                 (kv_lo + g / kResChunks) * kBlockN +
+                                     (g % kResChunks) * kResChunkCols,
                                  qt * kBlockM, bh);
                     tma_store_commit();
                     const bool next_ready =
@@ -460,9 +468,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int j = 0; j < n_kv; ++j) {
             const int sbuf = j & 1;
             const uint32_t tS = tmem + lane_base + sbuf * kBlockN;
-            const int key0 = j * kBlockN;
-            const bool diag = CAUSAL && (j == qt);
+            const int key0 = (kv_lo + j) * kBlockN;
+            const bool diag = CAUSAL && (kv_lo + j == qt);
             const bool ragged = key0 + kBlockN > p.N;
+            // Some row of the tile drops keys below its window start.
+            const bool wedge = CAUSAL && p.window > 0 && key0 < row_lo + kBlockM - p.window;
             // x ends up holding values whose row max commutes with a positive
             // factor `xmul` that turns them into log2-unit logits t; xmul then
             // folds into the exp2 FMA.  No residual: x is raw q.k and xmul the
@@ -546,11 +556,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     }
                 }
 
-                if (diag || ragged) {
+                if (diag || ragged || wedge) {
+                    const int klo = wedge ? q_row - p.window + 1 - key0 : -(1 << 30);   // first kept key
 #pragma unroll
                     for (int c = 0; c < kHalfN; ++c) {
                         const int key = col0 + c;
-                        const bool keep = (!diag || key <= r) && (key0 + key < p.N);
+                        const bool keep =
+                            (!diag || key <= r) && (key0 + key < p.N) && (key >= klo);
                         x[c] = keep ? x[c] : -INFINITY;
                     }
                 }
@@ -722,6 +734,7 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     prm.n_qtiles = (pb.N + kBlockM - 1) / kBlockM;
     prm.scale = pb.scale;
     prm.scale_log2 = pb.scale * kLog2e;
+    prm.window = pb.causal ? pb.window : 0;
     const unsigned grid = static_cast<unsigned>(prm.n_qtiles * BH);
     int ext = 0;
     if (pb.bias || pb.emit) {

@@ -19,6 +19,7 @@ struct FwdProblem {
     int B, Hq, Hkv, N, D;
     float scale;
     bool causal;
+    int window;      // sliding window W (causal only): key j kept iff i - W < j; 0 = none
 };
 
 // Validated backward problem.
@@ -29,6 +30,7 @@ struct BwdProblem {
     int B, Hq, Hkv, N, D;
     float scale;
     bool causal;
+    int window;      // as in FwdProblem
     float *dq_acc;   // fp32 [B,Hq,N,D] inside the workspace
     float *lse2;     // fp32 [B*Hq, NP]: LSE * log2(e), +inf on padding rows
     float *delta;    // fp32 [B*Hq, NP]: rowsum(dO * O), 0 on padding rows
