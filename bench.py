@@ -90,6 +90,8 @@ FWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_fwd.cu",
                "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
 BWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_bwd.cu",
                "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
+DEC_SOURCES = ["tiled_attention_02_gb300/csrc/attn_decode.cu",
+               "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
 
 
 def profiled_traffic(kernel_tag, digest, units):
@@ -304,6 +306,12 @@ EXTRA_WORKLOADS = {
                                N=16384, D=80, causal=True),
     "causal_fwd_bwd_d96": dict(name="causal_fwd_bwd_B1_H16_N16384_D96", B=1, Hq=16, Hkv=16,
                                N=16384, D=96, causal=True),
+    # Decode step (flash decode): one new query row per head over a 16384-row
+    # cache, grouped heads 32 : 8 (every K/V byte serves 4 query rows).
+    "decode": dict(name="decode_B16_H32_KV8_N16384_D128", kind="decode", B=16, Hq=32, Hkv=8,
+                   N=16384, D=128, causal=True),
+    "profile_decode_small": dict(name="decode_B4_H32_KV8_N16384_D128", kind="decode", B=4,
+                                 Hq=32, Hkv=8, N=16384, D=128, causal=True),
     # Causal sliding window of 4096 keys on the default step's shape.
     "swa_fwd_bwd": dict(name="swa4096_fwd_bwd_B1_H16_N16384_D128", B=1, Hq=16, Hkv=16, N=16384,
                         D=128, causal=True, window=4096),
@@ -348,7 +356,27 @@ def run_ours(args):
     # phases: list of (label, fn, flops, algorithmic bytes) run in order per step
     phases = []
     host_inputs, dev_inputs, results = [], [], []
-    if kind == "chain":
+    if kind == "decode":
+        from tiled_attention_02_gb300.inputs import make_decode
+        x = make_decode(B, Hq, Hkv, N, D, seed=rank)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(ta.attn_decode_workspace_size(B, Hq, Hkv, N, D), 256),
+                         dtype=torch.uint8, device=dev)
+
+        def dec():
+            s = ta.raw_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, Hq, Hkv, N, D, scale, ws.data_ptr(),
+                                   ws.numel(), sh)
+            assert s == 0, s
+        # algorithmic bytes: the K/V cache once, the query rows, O and LSE
+        dec_bytes = 2 * (B * Hkv * N * D) * 2 + 2 * (B * Hq * D) * 2 + B * Hq * 4
+        phases.append(("decode", dec, 4.0 * B * Hq * N * D, dec_bytes))
+        host_inputs += [x["q"], x["k"], x["v"]]
+        dev_inputs += [q, k, v]
+        results = [o]
+    elif kind == "chain":
         layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
         dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
         outs = [(torch.empty_like(x["q"]),
@@ -417,7 +445,7 @@ def run_ours(args):
             host_inputs.append(x["do"])
             dev_inputs.append(do)
             results = [dq, dk, dv]
-    launches = {"fwd": 1, "bwd": 3}
+    launches = {"fwd": 1, "bwd": 3, "decode": 2}
     launches_per_step = sum(launches.get(lbl, 1) for lbl, *_ in phases)
 
     def step():
@@ -501,6 +529,16 @@ def run_ours(args):
            + (f"_W{W['window']}" if W.get("window") else ""))
     kernels = {}
     for (lbl, _, fl, by), avg in zip(phases, ph_avg):
+        if kind == "decode":
+            ach = by / (avg * 1e-3) / 1e9
+            kernels[lbl] = {"kernel": f"decode_split_kernel<{D}> + decode_merge_kernel",
+                            "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                            "bytes_per_launch": by, "flops_per_launch": fl,
+                            "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
+                            "launches_timed": 2,
+                            "source_digest": source_digest(DEC_SOURCES)}
+            continue
         if kind == "chain":
             dg = source_digest(FWD_SOURCES)
             ach = by / (avg * 1e-3) / 1e9
@@ -538,6 +576,7 @@ def run_ours(args):
             "data": "synthetic: q,k,v(,dO) ~ N(0,1) bf16, seeded",
             "config": dict(config_block(world, W),
                            step={"fwd_bwd": "forward + backward", "fwd": "forward",
+                                 "decode": "one decode step (split keys, then merge)",
                                  "chain": "four chained forward layers, fp32 residual in place"}[kind]),
             "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
             "hbm_gbs_step": world * bytes_step / (ms_step * 1e-3) / 1e9,

@@ -219,6 +219,39 @@ attn_status attn_bwd_noalloc(const void *q, const void *k, const void *v, const 
                              int B, int Hq, int Hkv, int N, int D, float scale, int causal,
                              void *stream);
 
+/*
+ * Bytes of device workspace attn_decode needs: per (batch, query head) and
+ * per key split, an fp32 running max, row sum and D-column partial output
+ * (at most min(64, ceil(N/128)) splits), each region rounded up to 256
+ * bytes.  Returns 0 for an empty problem or invalid/unsupported sizes.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int N, int D);
+
+/*
+ * Decode step (flash decode): one new query row per (batch, query head)
+ * attends to an N-row key/value cache.  The query is at position N-1, so
+ * the causal mask keeps all N keys; the result equals the last row of
+ * attn_fwd with causal = 1 on the same cache.  The keys of each kv head are
+ * split over several thread blocks and the partial softmax states are merged
+ * with the online-softmax block-merge rule (kwkr.cn/news/592482, 2.2);
+ * "FlashAttention原理与Triton实战" section 7 names flash decode as an
+ * extension of the fused kernel.
+ *
+ *   q            bf16 [B,Hq,D]      the new query rows                 (in)
+ *   k, v         bf16 [B,Hkv,N,D]   key / value cache                  (in)
+ *   o            bf16 [B,Hq,D]      output rows                        (out)
+ *   lse          fp32 [B,Hq]        LSE of each row (natural log), or NULL (out)
+ *   scale        multiplier of q.k (usually 1/sqrt(D)); must be finite.
+ *   workspace    device scratch of at least attn_decode_workspace_size()
+ *                bytes, 256-byte aligned; contents on entry do not matter.
+ *
+ * D is 64, 80, 96 or 128; Hq / Hkv (query heads per kv head) at most 16
+ * (ATTN_ERR_UNSUPPORTED otherwise).  Other conventions as for attn_fwd.
+ */
+attn_status attn_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int Hq, int Hkv, int N, int D, float scale,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *attn_status_string(attn_status status);
 

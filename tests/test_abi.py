@@ -118,3 +118,27 @@ def test_window_entry_points_check_shapes_like_the_plain_ones(ta):
                                   None) == 0
     assert ta.raw_attn_bwd_window(A + 2, A, A, A, A, A, A, A, A, 1, 2, 2, 256, 64, 0.125, 64, A,
                                   1 << 30, None) == 1
+
+
+def test_decode_workspace_size(ta):
+    # splits: min(64, ceil(N/128)); m and l [rows, splits], o [rows, splits, D]
+    assert ta.attn_decode_workspace_size(1, 1, 1, 100, 64) == 256 + 256 + 256
+    assert ta.attn_decode_workspace_size(2, 8, 2, 16384, 128) == 2 * (16 * 64 * 4) + 16 * 64 * 128 * 4
+    assert ta.attn_decode_workspace_size(1, 32, 1, 1024, 64) == 0     # 32 query heads per kv head
+    assert ta.attn_decode_workspace_size(1, 2, 2, 1024, 72) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(o=A + 2), 1), (dict(ws=None), 1), (dict(ws=A + 16), 1),
+    (dict(ws_bytes=10), 1), (dict(D=72), 2), (dict(Hq=34, Hkv=2), 2), (dict(Hkv=3), 1),
+    (dict(scale=float("nan")), 1),
+])
+def test_decode_rejects_bad_arguments(ta, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=4, Hkv=2, N=1000, D=64, scale=0.125, ws=A,
+                ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    assert ta.raw_attn_decode(**args) == code
+
+
+def test_decode_empty_problem_is_ok(ta):
+    assert ta.raw_attn_decode(A, A, A, A, A, 0, 4, 2, 100, 64, 0.125, A, 1 << 30, None) == 0

@@ -1,0 +1,87 @@
+"""GPU parity of the decode step (attn_decode, flash decode) against the
+fp64 oracle: one query row per (batch, query head) at position N-1 over an
+N-row cache is the last row of causal attention."""
+import math
+
+import numpy as np
+import pytest
+
+from helpers import check_lse, check_o, to_oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ta():
+    import tiled_attention_02_gb300 as ta
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ta.build()
+    return ta
+
+
+def oracle_decode(orc, x, scale):
+    """Place each query row at position N-1 of an otherwise zero query
+    tensor and take the causal forward's last row."""
+    q = to_oracle(x["q"])
+    k, v = to_oracle(x["k"]), to_oracle(x["v"])
+    B, Hq, D = q.shape
+    N = k.shape[2]
+    qf = np.zeros((B, Hq, N, D))
+    qf[:, :, N - 1] = q
+    rows = np.arange(B * Hq) * N + (N - 1)
+    ref = orc.forward(qf, k, v, scale=scale, causal=True, rows=rows)
+    return ref["o"].reshape(B, Hq, D), ref["lse"].reshape(B, Hq)
+
+
+CASES = [
+    # B, Hq, Hkv, N, D
+    (1, 1, 1, 1, 64),          # a single key
+    (2, 4, 4, 100, 64),        # one ragged stage, plain multi-head
+    (2, 8, 2, 1000, 128),      # GQA 4:1, ragged
+    (1, 16, 1, 3000, 128),     # 16 query heads on one kv head
+    (3, 6, 2, 777, 80),        # D = 80
+    (2, 12, 4, 4096, 96),      # D = 96
+    (1, 5, 1, 20000, 128),     # long cache: many splits
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}H{c[1]}kv{c[2]}N{c[3]}D{c[4]}" for c in CASES])
+def test_decode_parity(ta, orc, case):
+    from tiled_attention_02_gb300.inputs import make_decode
+    B, Hq, Hkv, N, D = case
+    x = make_decode(B, Hq, Hkv, N, D, seed=N + D)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = ta.attn_decode(q, k, v)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    ro, rl = oracle_decode(orc, x, 1 / math.sqrt(D))
+    check_o(o, ro, f"decode {case}")
+    check_lse(lse, rl, f"decode {case}")
+
+
+def test_decode_equals_last_row_of_forward(ta):
+    """The decode kernel and the causal forward agree on the last row."""
+    from tiled_attention_02_gb300.inputs import make_qkv
+    B, Hq, Hkv, N, D = 1, 8, 2, 1500, 128
+    x = make_qkv(B, Hq, Hkv, N, D, seed=21)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    of, lf = ta.attn_fwd(q, k, v, causal=True)
+    od, ld = ta.attn_decode(q[:, :, N - 1].contiguous(), k, v)
+    torch.cuda.synchronize()
+    assert (of[:, :, N - 1].float() - od.float()).abs().max().item() <= 1.6e-2
+    assert (lf[:, :, N - 1] - ld).abs().max().item() <= 1e-3
+
+
+def test_decode_workspace_contents_do_not_matter(ta):
+    from tiled_attention_02_gb300.inputs import make_decode
+    B, Hq, Hkv, N, D = 2, 4, 2, 2000, 64
+    x = make_decode(B, Hq, Hkv, N, D, seed=4)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    need = ta.attn_decode_workspace_size(B, Hq, Hkv, N, D)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN patterns
+    o1, l1 = ta.attn_decode(q, k, v, workspace=ws)
+    o2, l2 = ta.attn_decode(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -33,7 +33,8 @@ ATTN_ERR_DEVICE_CHECK = 5
 
 # Every symbol include/tattn.h declares.
 EXPORTED = ("attn_fwd", "attn_fwd_window", "attn_bwd_workspace_size", "attn_bwd",
-            "attn_bwd_window", "attn_bwd_noalloc", "attn_status_string",
+            "attn_bwd_window", "attn_bwd_noalloc", "attn_decode_workspace_size", "attn_decode",
+            "attn_status_string",
             "attn_last_device_status", "attn_version")
 
 # Size of the fixed device scratch attn_bwd_noalloc uses (include/tattn.h).
@@ -80,6 +81,10 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                            f, i, vp]
             L.attn_bwd_noalloc.restype = i
+            L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
+            L.attn_decode_workspace_size.restype = sz
+            L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+            L.attn_decode.restype = i
             L.attn_status_string.argtypes = [i]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_last_device_status.argtypes = [vp]
@@ -261,6 +266,43 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, *, scale: float | None = None, causal:
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd_noalloc")
     return dq, dk, dv
+
+
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, N: int, D: int) -> int:
+    return int(lib().attn_decode_workspace_size(B, Hq, Hkv, N, D))
+
+
+def raw_attn_decode(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, ws, ws_bytes, stream) -> int:
+    return lib().attn_decode(q, k, v, o, lse, B, Hq, Hkv, N, D, ctypes.c_float(scale), ws,
+                             ws_bytes, stream)
+
+
+def attn_decode(q, k, v, *, scale: float | None = None, o=None, lse=None, want_lse: bool = True,
+                workspace=None, stream=None):
+    """Decode step through the C ABI: q [B,Hq,D] (one new row per query head)
+    against the cache k/v [B,Hkv,N,D].  Returns (o [B,Hq,D], lse [B,Hq])."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    _check(q, "q", torch.bfloat16, (B, Hq, D))
+    _check(k, "k", torch.bfloat16, (B, Hkv, N, D))
+    _check(v, "v", torch.bfloat16, (B, Hkv, N, D))
+    o = torch.empty_like(q) if o is None else o
+    _check(o, "o", torch.bfloat16, (B, Hq, D))
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lse, "lse", torch.float32, (B, Hq))
+    if workspace is None:
+        need = attn_decode_workspace_size(B, Hq, Hkv, N, D)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = raw_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D, scale,
+                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode")
+    return o, lse
 
 
 def attn_last_device_status(stream=None) -> int:

@@ -206,9 +206,80 @@ attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+struct DecWorkspace {
+    size_t m, l, o, total;
+};
+
+DecWorkspace decode_workspace_layout(int B, int Hq, int N, int D) {
+    auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t parts = static_cast<size_t>(B) * Hq * decode_max_splits(N);
+    DecWorkspace w;
+    w.m = 0;
+    w.l = round256(parts * sizeof(float));
+    w.o = w.l + round256(parts * sizeof(float));
+    w.total = w.o + round256(parts * D * sizeof(float));
+    return w;
+}
+
+constexpr int kDecodeMaxGroup = 16;
+
 }  // namespace
 
 extern "C" {
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int N, int D) {
+    bool empty = false;
+    if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
+    if (Hq / Hkv > kDecodeMaxGroup) return 0;
+    return decode_workspace_layout(B, Hq, N, D).total;
+}
+
+attn_status attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                        int Hq, int Hkv, int N, int D, float scale, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    bool empty = false;
+    attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (Hq / Hkv > kDecodeMaxGroup) return ATTN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !o || !workspace) return ATTN_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        (lse && !aligned(lse, 4)) || !aligned(workspace, 256))
+        return ATTN_ERR_INVALID;
+    const DecWorkspace wl = decode_workspace_layout(B, Hq, N, D);
+    if (workspace_bytes < wl.total) return ATTN_ERR_INVALID;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    // Split the keys so that about four blocks per SM run (one resident at a
+    // time), each over a whole number of 64-key stages.
+    const long long groups = static_cast<long long>(B) * Hkv;
+    long long s = (4LL * sms + groups - 1) / groups;
+    s = s < 1 ? 1 : (s > decode_max_splits(N) ? decode_max_splits(N) : s);
+    const int chunk = static_cast<int>(((N + s - 1) / s + 63) / 64 * 64);
+    DecProblem pb;
+    pb.q = q;
+    pb.k = k;
+    pb.v = v;
+    pb.o = o;
+    pb.lse = lse;
+    pb.B = B;
+    pb.Hq = Hq;
+    pb.Hkv = Hkv;
+    pb.N = N;
+    pb.D = D;
+    pb.scale = scale;
+    pb.chunk = chunk;
+    pb.splits = (N + chunk - 1) / chunk;
+    char *ws = static_cast<char *>(workspace);
+    pb.m_part = reinterpret_cast<float *>(ws + wl.m);
+    pb.l_part = reinterpret_cast<float *>(ws + wl.l);
+    pb.o_part = reinterpret_cast<float *>(ws + wl.o);
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    cudaError_t e = launch_decode(pb, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D) {
     bool empty = false;

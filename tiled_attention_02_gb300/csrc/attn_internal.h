@@ -37,6 +37,21 @@ struct BwdProblem {
     int NP;          // N rounded up to the 128-row tile
 };
 
+// Validated decode problem: one query row per (batch, query head) against an
+// N-row key/value cache, keys split over `splits` CTAs of `chunk` keys.
+struct DecProblem {
+    const void *q, *k, *v;   // q [B,Hq,D], k/v [B,Hkv,N,D] bf16
+    void *o;                 // [B,Hq,D] bf16
+    float *lse;              // [B,Hq] or null
+    int B, Hq, Hkv, N, D;
+    float scale;
+    int splits, chunk;
+    float *m_part, *l_part, *o_part;   // workspace: [B*Hq, splits] x2, [B*Hq, splits, D]
+};
+
+// Largest split count the decode workspace is sized for.
+int decode_max_splits(int N);
+
 // Byte offsets of the three workspace regions (each 256-byte aligned) and
 // the total size, for a validated shape.
 struct BwdWorkspace {
@@ -58,5 +73,6 @@ int *device_status_ptr();
 
 cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdProblem &pb, int *status, cudaStream_t stream);
+cudaError_t launch_decode(const DecProblem &pb, int *status, cudaStream_t stream);
 
 }  // namespace tattn

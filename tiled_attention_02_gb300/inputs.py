@@ -31,6 +31,15 @@ def make_qkv(B: int, Hq: int, Hkv: int, N: int, D: int, *, seed: int = 0,
     return out
 
 
+def make_decode(B: int, Hq: int, Hkv: int, N: int, D: int, *, seed: int = 0) -> dict:
+    """One query row per (batch, query head) and an N-row key/value cache:
+    q [B,Hq,D], k and v [B,Hkv,N,D] as bf16 CPU tensors."""
+    gen = torch.Generator().manual_seed(seed)
+    return {"q": _draw(gen, (B, Hq, D)),
+            "k": _draw(gen, (B, Hkv, N, D)),
+            "v": _draw(gen, (B, Hkv, N, D))}
+
+
 def make_chain(B: int, Hq: int, Hkv: int, N: int, D: int, *, layers: int = 4,
                seed: int = 0, with_do: bool = False) -> list[dict]:
     """Per-layer q, k, v for a block of chained layers, one generator."""
