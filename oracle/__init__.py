@@ -71,12 +71,12 @@ def _load():
                                          _dbl, ctypes.c_int, _i64, _ptr, _i64, ctypes.c_int,
                                          _ptr, _ptr, _ptr]
             lib.orc_delta_rows.argtypes = [_ptr, _ptr, _i64, _ptr, _i64, _ptr]
-            lib.orc_bwd_dq_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
-                                            _i64, _i64, _dbl, ctypes.c_int, _i64, _ptr, _i64,
-                                            _ptr]
-            lib.orc_bwd_dkv_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _i64,
-                                             _i64, _i64, _dbl, ctypes.c_int, _i64, _ptr, _i64,
-                                             _ptr, _ptr]
+            lib.orc_bwd_dq_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _i64,
+                                            _i64, _i64, _i64, _i64, _dbl, ctypes.c_int, _i64,
+                                            _ptr, _i64, _ptr, _ptr]
+            lib.orc_bwd_dkv_rows.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                                             _i64, _i64, _i64, _i64, _i64, _dbl, ctypes.c_int,
+                                             _i64, _ptr, _i64, _ptr, _ptr]
             _lib = lib
     return _lib
 
@@ -216,24 +216,44 @@ def delta(dO, o_rows, rows=None):
     return out
 
 
-def backward(q, k, v, dO, *, scale: float, causal: bool, window=None):
-    """Exact dQ, dK, dV (fp64) for every row; returns dict with o, lse too."""
+def backward(q, k, v, dO, *, scale: float, causal: bool, window=None, bias=None, grad_in=None):
+    """Exact dQ, dK, dV (fp64) for every row; returns dict with o, lse too.
+
+    bias [B,Hq,N,N] (the forward's additive logit bias) and grad_in
+    [B,Hq,N,N] (the gradient arriving at this layer's logits from the next
+    layer of a block residual chain) are optional.  With either given, the
+    result also holds ``dlogits`` [B,Hq,N,N]: the total logit gradient
+    dS = P o (dP - Delta) + grad_in on the kept keys and 0 elsewhere, which
+    is the gradient w.r.t. the bias and the ``grad_in`` of the previous
+    layer."""
     lib = _load()
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     B, Hq, Hkv, N, D = _shapes(q, k, v)
     w = _window(causal, window)
-    fw = forward(q, k, v, scale=scale, causal=causal, window=window)
+    bias = None if bias is None else _f64(bias)
+    grad_in = None if grad_in is None else _f64(grad_in)
+    for name, a in (("bias", bias), ("grad_in", grad_in)):
+        if a is not None and a.shape != (B, Hq, N, N):
+            raise ValueError(f"{name} must be [B,Hq,N,N]")
+    fw = forward(q, k, v, scale=scale, causal=causal, window=window, bias=bias)
     lse = np.ascontiguousarray(fw["lse"].reshape(-1))
     dlt = delta(dO, fw["o"].reshape(-1, D))
     dq = np.empty((B * Hq * N, D), dtype=np.float64)
     dk = np.empty((B * Hkv * N, D), dtype=np.float64)
     dv = np.empty((B * Hkv * N, D), dtype=np.float64)
-    lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                        float(scale), int(bool(causal)), w, None, B * Hq * N, _p(dq))
-    lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                         float(scale), int(bool(causal)), w, None, B * Hkv * N, _p(dk), _p(dv))
-    return {"o": fw["o"], "lse": fw["lse"], "dq": dq.reshape(B, Hq, N, D),
-            "dk": dk.reshape(B, Hkv, N, D), "dv": dv.reshape(B, Hkv, N, D)}
+    res = bias is not None or grad_in is not None
+    dl = np.empty((B * Hq * N, N), dtype=np.float64) if res else None
+    lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), _p(bias), _p(grad_in),
+                        B, Hq, Hkv, N, D, float(scale), int(bool(causal)), w, None, B * Hq * N,
+                        _p(dq), _p(dl))
+    lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), _p(bias), _p(grad_in),
+                         B, Hq, Hkv, N, D, float(scale), int(bool(causal)), w, None, B * Hkv * N,
+                         _p(dk), _p(dv))
+    out = {"o": fw["o"], "lse": fw["lse"], "dq": dq.reshape(B, Hq, N, D),
+           "dk": dk.reshape(B, Hkv, N, D), "dv": dv.reshape(B, Hkv, N, D)}
+    if res:
+        out["dlogits"] = dl.reshape(B, Hq, N, N)
+    return out
 
 
 def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows, window=None):
@@ -278,9 +298,11 @@ def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows,
     dk = np.empty((nk, D), dtype=np.float64)
     dv = np.empty((nk, D), dtype=np.float64)
     if nq:
-        lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                            float(scale), int(bool(causal)), w, _p(qr), nq, _p(dq))
+        lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), None, None, B, Hq,
+                            Hkv, N, D, float(scale), int(bool(causal)), w, _p(qr), nq, _p(dq),
+                            None)
     if nk:
-        lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, Hq, Hkv, N, D,
-                             float(scale), int(bool(causal)), w, _p(kr), nk, _p(dk), _p(dv))
+        lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), None, None, B, Hq,
+                             Hkv, N, D, float(scale), int(bool(causal)), w, _p(kr), nk, _p(dk),
+                             _p(dv))
     return {"dq": dq, "dk": dk, "dv": dv}

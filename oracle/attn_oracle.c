@@ -194,15 +194,24 @@ void orc_delta_rows(const double *dO, const double *o, int64_t D,
 }
 
 /*
- * dQ for the listed query rows (no bias; the backward has none).
+ * dQ for the listed query rows.
  *   lse, delta: full [B,Hq,N] arrays, read at the listed rows only.
- *   dq [nrows, D].
+ *   bias:    [B,Hq,N,N] or NULL, the additive logit bias of the forward.
+ *   grad_in: [B,Hq,N,N] or NULL, the gradient flowing into this layer's
+ *            logits from the next layer of a block residual chain (the next
+ *            layer adds these logits to its own, unscaled, so its total
+ *            logit gradient arrives here unchanged).
+ *   dq [nrows, D];  grad_out [nrows, N] or NULL: the total logit gradient
+ *   dS_ij for j in J_i (also the gradient of the loss w.r.t. bias_ij),
+ *   0 for the keys outside J_i.
+ * With both NULL this is the plain attention backward.
  */
 void orc_bwd_dq_rows(const double *q, const double *k, const double *v, const double *dO,
-                     const double *lse, const double *delta,
+                     const double *lse, const double *delta, const double *bias,
+                     const double *grad_in,
                      int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t D,
                      double scale, int causal, int64_t window, const int64_t *rows,
-                     int64_t nrows, double *dq)
+                     int64_t nrows, double *dq, double *grad_out)
 {
     (void)B;
     const int64_t group = Hq / Hkv;
@@ -223,18 +232,23 @@ void orc_bwd_dq_rows(const double *q, const double *k, const double *v, const do
             key_range(i, N, causal, window, &j0, &j1);
             const int64_t nk = j1 - j0;
 
-            row_logits(q + flat * D, k_head + j0 * D, NULL, nk, D, scale, s);
+            row_logits(q + flat * D, k_head + j0 * D, bias ? bias + flat * N + j0 : NULL, nk, D,
+                       scale, s);
             double *dq_row = dq + r * D;
             for (int64_t d = 0; d < D; ++d) dq_row[d] = 0.0;
+            double *go = grad_out ? grad_out + r * N : NULL;
+            if (go)
+                for (int64_t j = 0; j < N; ++j) go[j] = 0.0;
             for (int64_t t = 0; t < nk; ++t) {
                 const int64_t j = j0 + t;
                 const double p = exp(s[t] - lse[flat]);
                 double dp = 0.0;
                 for (int64_t d = 0; d < D; ++d)
                     dp += do_row[d] * v_head[j * D + d];
-                const double ds = p * (dp - delta[flat]);
+                const double ds = p * (dp - delta[flat]) + (grad_in ? grad_in[flat * N + j] : 0.0);
                 for (int64_t d = 0; d < D; ++d)
                     dq_row[d] += scale * ds * k_head[j * D + d];
+                if (go) go[j] = ds;
             }
         }
         free(s);
@@ -244,11 +258,13 @@ void orc_bwd_dq_rows(const double *q, const double *k, const double *v, const do
 /*
  * dK and dV for the listed key rows; key row flat index (b*Hkv + g)*N + j.
  * Sums over every query head of the group and every query row i with
- * j in J_i.  lse, delta: full [B,Hq,N] arrays, read for the rows involved.
+ * j in J_i.  lse, delta: full [B,Hq,N] arrays, read for the rows involved;
+ * bias and grad_in as for orc_bwd_dq_rows (or NULL).
  *   dk, dv [nkrows, D].
  */
 void orc_bwd_dkv_rows(const double *q, const double *k, const double *v, const double *dO,
-                      const double *lse, const double *delta,
+                      const double *lse, const double *delta, const double *bias,
+                      const double *grad_in,
                       int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t D,
                       double scale, int causal, int64_t window, const int64_t *krows,
                       int64_t nkrows, double *dk, double *dv)
@@ -280,8 +296,9 @@ void orc_bwd_dkv_rows(const double *q, const double *k, const double *v, const d
                     dot += q_row[d] * k_row[d];
                     dp += do_row[d] * v_row[d];
                 }
-                const double p = exp(scale * dot - lse[qflat]);
-                const double ds = p * (dp - delta[qflat]);
+                const double b_ij = bias ? bias[qflat * N + j] : 0.0;
+                const double p = exp(scale * dot + b_ij - lse[qflat]);
+                const double ds = p * (dp - delta[qflat]) + (grad_in ? grad_in[qflat * N + j] : 0.0);
                 for (int64_t d = 0; d < D; ++d) {
                     dv_row[d] += p * do_row[d];
                     dk_row[d] += scale * ds * q_row[d];

@@ -31,9 +31,13 @@ MUTANTS = [
     ("no_max_subtraction", "const double p = exp(s[t] - m) / l;", "const double p = exp(s[t]) / l;"),
     ("lse_base2", "if (lse) lse[r] = m + log(l);", "if (lse) lse[r] = m + log2(l);"),
     ("lse_missing_max", "if (lse) lse[r] = m + log(l);", "if (lse) lse[r] = log(l);"),
-    ("ds_sign_dq", "const double ds = p * (dp - delta[flat]);", "const double ds = p * (delta[flat] - dp);"),
-    ("ds_sign_dk", "const double ds = p * (dp - delta[qflat]);", "const double ds = p * (delta[qflat] - dp);"),
-    ("dq_missing_delta", "const double ds = p * (dp - delta[flat]);", "const double ds = p * dp;"),
+    ("ds_sign_dq", "const double ds = p * (dp - delta[flat]) +", "const double ds = p * (delta[flat] - dp) +"),
+    ("ds_sign_dk", "const double ds = p * (dp - delta[qflat]) +", "const double ds = p * (delta[qflat] - dp) +"),
+    ("dq_missing_delta", "const double ds = p * (dp - delta[flat]) +", "const double ds = p * dp +"),
+    ("dq_drops_grad_in", "(grad_in ? grad_in[flat * N + j] : 0.0);", "0.0;"),
+    ("dkv_drops_bias", "const double b_ij = bias ? bias[qflat * N + j] : 0.0;", "const double b_ij = 0.0;"),
+    ("dkv_grad_in_transposed", "(grad_in ? grad_in[qflat * N + j] : 0.0);",
+     "(grad_in ? grad_in[(qflat - i + j) * N + i] : 0.0);"),
     ("dq_missing_scale", "dq_row[d] += scale * ds * k_head[j * D + d];", "dq_row[d] += ds * k_head[j * D + d];"),
     ("dk_transposed_operand", "dk_row[d] += scale * ds * q_row[d];", "dk_row[d] += scale * ds * do_row[d];"),
     ("dv_uses_ds", "dv_row[d] += p * do_row[d];", "dv_row[d] += ds * do_row[d];"),

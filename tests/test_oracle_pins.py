@@ -504,3 +504,80 @@ def test_window_needs_causal(orc):
         orc.forward(x, x, x, scale=1.0, causal=False, window=2)
     with pytest.raises(ValueError):
         orc.forward(x, x, x, scale=1.0, causal=True, window=0)
+
+
+# ------------------------------------------- block-residual backward
+# Reading ([BlockRes] "v1: Fuse Residual 进 Attention Kernel": the backward
+# keeps the LSE statistics, corrected for the residual; no formula printed):
+# S_l = scale Q_l K_l^T + S_{l-1}.  S_l reaches the loss through layer l's
+# softmax and, unscaled, through S_{l+1}, so the total logit gradient is
+# dS_l = P_l o (dP_l - Delta_l) + dS_{l+1}; it drives dQ_l, dK_l and is the
+# gradient of layer l's bias.
+
+def chain_forward(orc, layers, scale, causal):
+    outs, prev = [], None
+    for q, k, v in layers:
+        f = orc.forward(q, k, v, scale=scale, causal=causal,
+                        bias=None if prev is None else np.nan_to_num(prev), emit_logits=True)
+        outs.append(f["o"])
+        prev = f["logits"]
+    return outs
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_residual_chain_backward_matches_finite_differences(orc, causal):
+    """Two chained layers, L = sum_l sum(O_l * dO_l): layer 1's backward with
+    bias S_0 gives dlogits_1, which enters layer 0's backward as grad_in;
+    every input's gradient must equal central differences of L."""
+    B, Hq, Hkv, N, D = 1, 2, 1, 5, 3
+    scale = 0.7
+    layers = [(rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D)) for _ in range(2)]
+    dos = [rand(B, Hq, N, D) for _ in range(2)]
+
+    def L(ls):
+        return float(sum((o * do).sum() for o, do in zip(chain_forward(orc, ls, scale, causal), dos)))
+
+    f0 = orc.forward(*layers[0], scale=scale, causal=causal, emit_logits=True)
+    g1 = orc.backward(*layers[1], dos[1], scale=scale, causal=causal,
+                      bias=np.nan_to_num(f0["logits"]))
+    g0 = orc.backward(*layers[0], dos[0], scale=scale, causal=causal, grad_in=g1["dlogits"])
+    grads = [g0, g1]
+    h = 1e-5
+    for li in range(2):
+        for ti, name in enumerate(("dq", "dk", "dv")):
+            arr = layers[li][ti]
+            fd = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                a = arr.copy(); a[idx] += h
+                b = arr.copy(); b[idx] -= h
+                lp = [list(x) for x in layers]; lp[li][ti] = a
+                lm = [list(x) for x in layers]; lm[li][ti] = b
+                fd[idx] = (L(lp) - L(lm)) / (2 * h)
+            err = np.abs(grads[li][name] - fd).max() / max(1.0, np.abs(fd).max())
+            assert err < 1e-7, (li, name, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bias_gradient_is_total_logit_gradient(orc, causal):
+    """dL/dbias_ij by central differences equals dlogits on the kept keys
+    and 0 on the masked ones; grad_in adds straight onto it."""
+    B, H, N, D = 1, 1, 4, 3
+    q, k, v, do = rand(B, H, N, D), rand(B, H, N, D), rand(B, H, N, D), rand(B, H, N, D)
+    bias, gin = rand(B, H, N, N), rand(B, H, N, N)
+
+    def L(bb):
+        return float((orc.forward(q, k, v, scale=0.5, causal=causal, bias=bb)["o"] * do).sum())
+
+    g = orc.backward(q, k, v, do, scale=0.5, causal=causal, bias=bias)
+    h = 1e-6
+    fd = np.zeros_like(bias)
+    for idx in np.ndindex(bias.shape):
+        a = bias.copy(); a[idx] += h
+        b = bias.copy(); b[idx] -= h
+        fd[idx] = (L(a) - L(b)) / (2 * h)
+    np.testing.assert_allclose(g["dlogits"], fd, rtol=0, atol=1e-8)
+    g2 = orc.backward(q, k, v, do, scale=0.5, causal=causal, bias=bias, grad_in=gin)
+    kept = np.tril(np.ones((N, N), dtype=bool)) if causal else np.ones((N, N), dtype=bool)
+    np.testing.assert_allclose(g2["dlogits"][..., kept], (g["dlogits"] + gin)[..., kept],
+                               rtol=0, atol=1e-14)
+    assert (g2["dlogits"][..., ~kept] == 0).all()
