@@ -284,7 +284,7 @@ def config_block(world, W=None):
            "D": W["D"], "causal": W["causal"], "scale": 1 / math.sqrt(W["D"]),
            "parallelism": f"replicas x{world} (independent problems, no collective)",
            "l2": "flushed between timed steps (256 MB write)"}
-    if W.get("kind") == "chain":
+    if W.get("kind") in ("chain", "chain_train"):
         cfg["layers"] = W["layers"]
     if W.get("window"):
         cfg["window"] = W["window"]
@@ -306,6 +306,10 @@ EXTRA_WORKLOADS = {
                                N=16384, D=80, causal=True),
     "causal_fwd_bwd_d96": dict(name="causal_fwd_bwd_B1_H16_N16384_D96", B=1, Hq=16, Hkv=16,
                                N=16384, D=96, causal=True),
+    # Training step of the block residual chain: 4 layers forward, 4 backward.
+    "residual_chain_train": dict(name="residual_chain_train_4layers_B1_H20_KV4_N4096_D128",
+                                 kind="chain_train", layers=4, B=1, Hq=20, Hkv=4, N=4096, D=128,
+                                 causal=True),
     # Decode step (flash decode): one new query row per head over a 16384-row
     # cache, grouped heads 32 : 8 (every K/V byte serves 4 query rows).
     "decode": dict(name="decode_B16_H32_KV8_N16384_D128", kind="decode", B=16, Hq=32, Hkv=8,
@@ -376,6 +380,51 @@ def run_ours(args):
         host_inputs += [x["q"], x["k"], x["v"]]
         dev_inputs += [q, k, v]
         results = [o]
+    elif kind == "chain_train":
+        # 4-layer block, forward then backward: every layer keeps its emitted
+        # logits (the next layer's bias, needed again by the backward), and
+        # one fp32 buffer carries the logit gradient down the block in place.
+        L = W["layers"]
+        layers = make_chain(B, Hq, Hkv, N, D, layers=L, seed=rank, with_do=True)
+        dl = [{n: x[n].to(dev) for n in ("q", "k", "v", "do")} for x in layers]
+        outs = [(torch.empty_like(x["q"]),
+                 torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
+        S = [torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev) for _ in range(L - 1)]
+        gbuf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
+        grads = [(torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
+                 for x in dl]
+        ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+                         dtype=torch.uint8, device=dev)
+        kept = B * Hq * (N * (N + 1) // 2 if causal else N * N) * 4
+        for i in range(L):
+            def layer_f(i=i):
+                x, (o, lse) = dl[i], outs[i]
+                st = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                     S[i - 1].data_ptr() if i > 0 else None, o.data_ptr(),
+                                     lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                     S[i].data_ptr() if i < L - 1 else None, sh)
+                assert st == 0, st
+            phases.append((f"fwd{i}", layer_f, attn_flops(B, Hq, N, D, causal),
+                           chain_layer_bytes(W, i)))
+        io_b = 5 * (B * Hq * N * D) * 2 + 2 * 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+        for i in reversed(range(L)):
+            def layer_b(i=i):
+                x, (o, lse) = dl[i], outs[i]
+                dq, dk, dv = grads[i]
+                st = ta.raw_attn_bwd_residual(
+                    x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
+                    lse.data_ptr(), x["do"].data_ptr(), S[i - 1].data_ptr() if i > 0 else None,
+                    gbuf.data_ptr() if i < L - 1 else None, dq.data_ptr(), dk.data_ptr(),
+                    dv.data_ptr(), gbuf.data_ptr() if i > 0 else None, B, Hq, Hkv, N, D, scale,
+                    causal, ws.data_ptr(), ws.numel(), sh)
+                assert st == 0, st
+            by = io_b + kept * ((i > 0) + (i < L - 1) + (i > 0))
+            phases.append((f"bwd{i}", layer_b, bwd_flops(B, Hq, N, D, causal), by))
+        for i, x in enumerate(layers):
+            for n in ("q", "k", "v", "do"):
+                host_inputs.append(x[n])
+                dev_inputs.append(dl[i][n])
+        results = [grads[0][0]]
     elif kind == "chain":
         layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
         dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
@@ -446,6 +495,7 @@ def run_ours(args):
             dev_inputs.append(do)
             results = [dq, dk, dv]
     launches = {"fwd": 1, "bwd": 3, "decode": 2}
+    launches.update({f"bwd{i}": 3 for i in range(8)})
     launches_per_step = sum(launches.get(lbl, 1) for lbl, *_ in phases)
 
     def step():
@@ -539,6 +589,18 @@ def run_ours(args):
                             "launches_timed": 2,
                             "source_digest": source_digest(DEC_SOURCES)}
             continue
+        if kind == "chain_train":
+            is_b = lbl.startswith("bwd")
+            dg = source_digest(BWD_SOURCES if is_b else FWD_SOURCES)
+            ach = by / (avg * 1e-3) / 1e9
+            kernels[lbl] = {"kernel": ("bwd_main_kernel<%d,causal,residual> (+pre, dQ convert)" % D
+                                       if is_b else f"fwd_kernel<{D},causal,bias/emit>"),
+                            "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                            "bytes_per_launch": by, "flops_per_launch": fl,
+                            "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
+                            "launches_timed": 3 if is_b else 1, "source_digest": dg}
+            continue
         if kind == "chain":
             dg = source_digest(FWD_SOURCES)
             ach = by / (avg * 1e-3) / 1e9
@@ -577,6 +639,8 @@ def run_ours(args):
             "config": dict(config_block(world, W),
                            step={"fwd_bwd": "forward + backward", "fwd": "forward",
                                  "decode": "one decode step (split keys, then merge)",
+                                 "chain_train": "four chained layers forward, then backward "
+                                                "through the block (fp32 residual and gradient)",
                                  "chain": "four chained forward layers, fp32 residual in place"}[kind]),
             "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
             "hbm_gbs_step": world * bytes_step / (ms_step * 1e-3) / 1e9,

@@ -166,6 +166,39 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass of one layer of a block attention residual chain.
+ *
+ * The layer computed  S = scale QK^T + bias  (bias = the previous layer's
+ * emitted logits, or none for the first layer of a block) and, when it is
+ * not the last layer, emitted S to the next layer, whose own logits add S
+ * unscaled.  The gradient reaching S is therefore
+ *     dS = P o (dP - Delta) + grad_in
+ * (grad_in = the next layer's dS, absent for the last layer); dS gives
+ * dq = scale dS K and dk = scale dS^T Q, dv = P^T dO, and dS itself is the
+ * gradient of the bias, written to grad_out for the previous layer.  The
+ * Block Attention Residual page ("v1: Fuse Residual 进 Attention Kernel")
+ * says the backward keeps the LSE statistics, corrected for the residual:
+ * lse must be the one attn_fwd returned with this bias.
+ *
+ *   bias      fp32 [B,Hq,N,N] the forward's bias, or NULL              (in)
+ *   grad_in   fp32 [B,Hq,N,N] incoming logit gradient, or NULL         (in)
+ *   grad_out  fp32 [B,Hq,N,N] dS on the kept entries, or NULL          (out)
+ *             MAY be the same pointer as grad_in (in-place chain buffer):
+ *             each element is read by the only thread block that later
+ *             writes it.  Under the causal mask, tiles above the diagonal
+ *             are not touched; masked entries inside the diagonal tiles
+ *             hold unspecified values and are never read as grad_in.
+ * Other arguments, layouts, workspace and errors are those of attn_bwd.
+ * The residual tensors need 16-byte aligned bases and N % 4 == 0
+ * (ATTN_ERR_UNSUPPORTED otherwise).
+ */
+attn_status attn_bwd_residual(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dO, const float *bias,
+                              const float *grad_in, void *dq, void *dk, void *dv, float *grad_out,
+                              int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Backward pass of attn_fwd_window (same q, k, v, scale and window; no bias).
  * Arguments, workspace, layouts and errors are those of attn_bwd with
  * causal = 1, plus window >= 1 as in attn_fwd_window.

@@ -142,3 +142,21 @@ def test_decode_rejects_bad_arguments(ta, kw, code):
 
 def test_decode_empty_problem_is_ok(ta):
     assert ta.raw_attn_decode(A, A, A, A, A, 0, 4, 2, 100, 64, 0.125, A, 1 << 30, None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=254), 2),            # residual rows must be 16-byte multiples
+    (dict(bias=A + 4), 2),       # 16-byte aligned residual bases
+    (dict(gout=A + 2), 1),       # fp32 alignment
+    (dict(D=72), 2), (dict(lse=None), 1),
+])
+def test_bwd_residual_rejects(ta, kw, code):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, do=A, bias=A, gin=A, dq=A, dk=A, dv=A, gout=A, B=1,
+                Hq=2, Hkv=2, N=256, D=64, scale=0.125, causal=1, ws=A, ws_bytes=1 << 30,
+                stream=None)
+    args.update(kw)
+    assert ta.raw_attn_bwd_residual(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                    args["do"], args["bias"], args["gin"], args["dq"], args["dk"],
+                                    args["dv"], args["gout"], args["B"], args["Hq"], args["Hkv"],
+                                    args["N"], args["D"], args["scale"], args["causal"],
+                                    args["ws"], args["ws_bytes"], args["stream"]) == code

@@ -33,7 +33,7 @@ ATTN_ERR_DEVICE_CHECK = 5
 
 # Every symbol include/tattn.h declares.
 EXPORTED = ("attn_fwd", "attn_fwd_window", "attn_bwd_workspace_size", "attn_bwd",
-            "attn_bwd_window", "attn_bwd_noalloc", "attn_decode_workspace_size", "attn_decode",
+            "attn_bwd_window", "attn_bwd_residual", "attn_bwd_noalloc", "attn_decode_workspace_size", "attn_decode",
             "attn_status_string",
             "attn_last_device_status", "attn_version")
 
@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
                                           i, vp, sz, vp]
             L.attn_bwd_window.restype = i
+            L.attn_bwd_residual.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i,
+                                            i, i, i, f, i, vp, sz, vp]
+            L.attn_bwd_residual.restype = i
             L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                            f, i, vp]
             L.attn_bwd_noalloc.restype = i
@@ -144,6 +147,13 @@ def raw_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D, scale, causa
                           ctypes.c_float(scale), int(causal), ws, ws_bytes, stream)
 
 
+def raw_attn_bwd_residual(q, k, v, o, lse, do, bias, grad_in, dq, dk, dv, grad_out, B, Hq, Hkv,
+                          N, D, scale, causal, ws, ws_bytes, stream) -> int:
+    return lib().attn_bwd_residual(q, k, v, o, lse, do, bias, grad_in, dq, dk, dv, grad_out, B,
+                                   Hq, Hkv, N, D, ctypes.c_float(scale), int(causal), ws,
+                                   ws_bytes, stream)
+
+
 def raw_attn_bwd_window(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D, scale, window, ws,
                         ws_bytes, stream) -> int:
     return lib().attn_bwd_window(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D,
@@ -197,8 +207,13 @@ def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, D: int) -> int:
 
 def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = False,
              dq=None, dk=None, dv=None, workspace=None, stream=None,
-             window: int | None = None):
-    """Backward by recomputation through the C ABI; returns (dq, dk, dv)."""
+             window: int | None = None, bias=None, grad_in=None, grad_out=None):
+    """Backward by recomputation through the C ABI; returns (dq, dk, dv).
+
+    Block attention residual (attn_bwd_residual): ``bias`` is the forward's
+    fp32 [B,Hq,N,N] logit bias, ``grad_in`` the gradient arriving at this
+    layer's logits from the next layer, and ``grad_out`` (may be grad_in)
+    receives this layer's total logit gradient."""
     import torch
     B, Hq, N, D = q.shape
     Hkv = k.shape[1]
@@ -218,7 +233,16 @@ def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = 
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    if window is not None:
+    if bias is not None or grad_in is not None or grad_out is not None:
+        if window is not None:
+            raise ValueError("the residual backward takes no window")
+        for t, name in ((bias, "bias"), (grad_in, "grad_in"), (grad_out, "grad_out")):
+            _check(t, name, torch.float32, (B, Hq, N, N))
+        st = raw_attn_bwd_residual(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                   _ptr(bias), _ptr(grad_in), _ptr(dq), _ptr(dk), _ptr(dv),
+                                   _ptr(grad_out), B, Hq, Hkv, N, D, scale, causal,
+                                   _ptr(workspace), ws_bytes, _stream_handle(stream))
+    elif window is not None:
         if not causal:
             raise ValueError("a sliding window needs causal=True")
         st = raw_attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),

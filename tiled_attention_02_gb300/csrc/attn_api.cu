@@ -164,7 +164,8 @@ attn_status fwd_impl(const void *q, const void *k, const void *v, const float *b
 attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const float *lse,
                      const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N,
                      int D, float scale, int causal, int window, void *workspace,
-                     size_t workspace_bytes, void *stream) {
+                     size_t workspace_bytes, void *stream, const float *bias = nullptr,
+                     const float *grad_in = nullptr, float *grad_out = nullptr) {
     bool empty = false;
     attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
     if (st != ATTN_OK || empty) return st;
@@ -174,6 +175,16 @@ attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
     for (const void *p : bf)
         if (!aligned(p, 16)) return ATTN_ERR_INVALID;
     if (!aligned(lse, 4) || !aligned(workspace, 256)) return ATTN_ERR_INVALID;
+    if (bias || grad_in || grad_out) {
+        const float *res[3] = {bias, grad_in, grad_out};
+        for (const float *r : res)
+            if (r && !aligned(r, 4)) return ATTN_ERR_INVALID;
+        // The residual tiles move as TMA boxes: 16-byte rows and bases.
+        for (const float *r : res)
+            if (r && (!aligned(r, 16) || N % 4 != 0)) return ATTN_ERR_UNSUPPORTED;
+        const double elems = static_cast<double>(B) * Hq * static_cast<double>(N) * N;
+        if (elems > 9.0e18) return ATTN_ERR_UNSUPPORTED;
+    }
     const BwdWorkspace wl = bwd_workspace_layout(B, Hq, N, D);
     if (workspace_bytes < wl.total) return ATTN_ERR_INVALID;
     BwdProblem pb;
@@ -194,6 +205,9 @@ attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
     pb.scale = scale;
     pb.causal = causal != 0;
     pb.window = (window > 0 && window < N) ? window : 0;
+    pb.bias = bias;
+    pb.grad_in = grad_in;
+    pb.grad_out = grad_out;
     char *ws = static_cast<char *>(workspace);
     pb.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
     pb.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
@@ -308,6 +322,15 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      void *stream) {
     return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal, 0,
                     workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_residual(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dO, const float *bias,
+                              const float *grad_in, void *dq, void *dk, void *dv, float *grad_out,
+                              int B, int Hq, int Hkv, int N, int D, float scale, int causal,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal, 0,
+                    workspace, workspace_bytes, stream, bias, grad_in, grad_out);
 }
 
 attn_status attn_bwd_window(const void *q, const void *k, const void *v, const void *o,

@@ -112,10 +112,19 @@ bwd_dq_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, siz
 
 // ------------------------------------------------------------ main kernel
 
-constexpr int kThreads = 448;
 constexpr int kMaxSmem = 232448;   // opt-in shared memory per block on sm_100/sm_103
+// Block residual variant: fp32 [query][key] tiles of the bias, the incoming
+// logit gradient and the outgoing one move in chunks of 32 query rows x 128
+// keys (four 32 x 32 boxes of 128-byte swizzled rows).
+constexpr int kResQ = 32;                      // query rows per chunk
+constexpr int kResChunkBytes = kResQ * kTile * 4;
+constexpr int kResChunks = kTile / kResQ;      // chunks per (query tile, key tile)
+constexpr int kResSlots = 4;
 
-template <int D>
+template <bool RES>
+constexpr int bwd_threads() { return RES ? 512 : 448; }
+
+template <int D, bool RES = false>
 struct BwdCfg {
     // A bf16 row of D elements occupies ceil(D/64) 128-byte swizzle atoms
     // (zero-filled past D by TMA); stores and reductions are clipped at D.
@@ -123,14 +132,20 @@ struct BwdCfg {
     static constexpr int kChunkBytes = kTile * 128;
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kDQBoxes = (D + 31) / 32;   // fp32 dQ boxes of 32 columns
+    // The residual variant keeps one {Q, dO} stage and gives the other's
+    // shared memory to its fp32 chunk ring.
+    static constexpr int kQStages = RES ? 1 : 2;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTileBytes;
-    static constexpr int kOffStage = 2 * kTileBytes;          // 2 stages of {Q, dO}
+    static constexpr int kOffStage = 2 * kTileBytes;          // kQStages stages of {Q, dO}
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kOffRows = kOffStage + 2 * kStageBytes;   // lse2[2][128], delta[2][128]
+    static constexpr int kOffRows = kOffStage + kQStages * kStageBytes;   // lse2[2][128], delta[2][128]
     static constexpr int kOffDS = ((kOffRows + 4 * kTile * 4) + 1023) & ~1023;
     static constexpr int kDSBytes = kTile * kTile * 2;
-    static constexpr int kOffBar = kOffDS + kDSBytes;
+    static constexpr int kOffRes = kOffDS + kDSBytes;
+    static constexpr int kNumResSlots = RES ? kResSlots : 0;
+    static constexpr int kResRing = RES ? kResSlots : 1;
+    static constexpr int kOffBar = kOffRes + kNumResSlots * kResChunkBytes;
     static constexpr int kBarKV = 0;
     static constexpr int kBarQDFull = 1;     // 2
     static constexpr int kBarQDEmpty = 3;    // 2
@@ -143,7 +158,10 @@ struct BwdCfg {
     static constexpr int kBarDSFree = 11;
     static constexpr int kBarAccDone = 12;
     static constexpr int kBarDrain = 13;
-    static constexpr int kNumBars = 14;
+    static constexpr int kBarResFull = 14;                        // kNumResSlots each
+    static constexpr int kBarResDone = kBarResFull + kNumResSlots;
+    static constexpr int kBarResFree = kBarResDone + kNumResSlots;
+    static constexpr int kNumBars = kBarResFree + kNumResSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kUsed = kOffMisc + 16;
     static constexpr int kSmemBytes = (kUsed + 1023 <= kMaxSmem) ? kUsed + 1023 : kMaxSmem;
@@ -152,6 +170,7 @@ struct BwdCfg {
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
     static constexpr uint32_t kColDK = D <= 64 ? 256 + 64 : 384;
     static_assert(kDQBoxes * kTile * 128 <= 2 * kTileBytes, "dQ staging fits a stage");
+    static_assert(kResChunks == 4, "one chunk per P/dS warpgroup half");
     static_assert(kUsed <= kMaxSmem, "shared memory budget");
 };
 
@@ -163,6 +182,8 @@ struct BwdParams {
     int N, NP, Hq, Hkv, group, BHkv, n_tiles;
     float scale, scale_log2;
     int window;   // causal sliding window W (key j kept for query i iff i - W < j), 0 = none
+    // residual variant: which of the three fp32 [B,Hq,N,N] tensors are given
+    int has_bias, has_gin, has_gout;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -193,13 +214,15 @@ __device__ __forceinline__ void stage_row64(uint32_t tile, int r, int atom, cons
     }
 }
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, bool RES>
+__global__ void __launch_bounds__(bwd_threads<RES>(), 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
-    using C = BwdCfg<D>;
+                const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmBias,
+                const __grid_constant__ CUtensorMap tmGin, const __grid_constant__ CUtensorMap tmGout,
+                const BwdParams p) {
+    using C = BwdCfg<D, RES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -233,6 +256,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto item_qi = [&](int j) { return q_lo + j % nq; };
     auto item_bhq = [&](int j) { return b * p.Hq + g * p.group + j / nq; };
     const uint32_t s_rows = sb + C::kOffRows;   // lse2[s][128] then delta[s][128]
+    // Residual chunk sequence of item j: the bias chunks c = 0..3 (if a bias
+    // is given), then the logit-gradient chunks c = 0..3 (if one flows in or
+    // out); chunk c covers query rows 32c..32c+31 of the item's query tile.
+    const int res_bias = RES && p.has_bias ? kResChunks : 0;
+    const int res_grad = RES && (p.has_gin || p.has_gout) ? kResChunks : 0;
+    const int res_per_item = res_bias + res_grad;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -240,6 +269,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::kBarQDFull + s), 1);
             mbar_init(bar(C::kBarQDEmpty + s), 1);
+        }
+        for (int s = 0; s < C::kNumResSlots; ++s) {
+            mbar_init(bar(C::kBarResFull + s), 1);
+            mbar_init(bar(C::kBarResDone + s), kTile);   // one P/dS warpgroup per chunk
+            mbar_init(bar(C::kBarResFree + s), 1);
         }
         mbar_init(bar(C::kBarSFull), 1);
         mbar_init(bar(C::kBarDPFull), 1);
@@ -274,8 +308,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             int issued = 0;
             for (int j = 0; j < n_items; ++j) {
-                const int s = j & 1;
-                if (j >= 2) ok = mbar_wait(bar(C::kBarQDEmpty + s), ((j >> 1) - 1) & 1, ac);
+                const int s = j % C::kQStages;
+                if (j >= C::kQStages)
+                    ok = mbar_wait(bar(C::kBarQDEmpty + s), ((j / C::kQStages) - 1) & 1, ac);
                 if (!ok) break;
                 const int qi = item_qi(j), bhq = item_bhq(j);
                 const uint32_t fb = bar(C::kBarQDFull + s);
@@ -293,8 +328,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             if (!ok) {
                 drain_wait(bar(C::kBarKV), 0);
-                for (int j = max(issued - 2, 0); j < issued; ++j)
-                    drain_wait(bar(C::kBarQDFull + (j & 1)), (j >> 1) & 1);
+                for (int j = max(issued - C::kQStages, 0); j < issued; ++j)
+                    drain_wait(bar(C::kBarQDFull + j % C::kQStages), (j / C::kQStages) & 1);
             }
         }
         __syncwarp();
@@ -309,8 +344,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // Order per query tile j:
                 //   S^T(j)  dP^T(j)  [P_ready] dV(j)  [dS_ready] dK(j)  dQ(j)
                 // P is computed while dP^T runs and dS while dV runs.
-                const int s = j & 1;
-                if (!(ok = mbar_wait(bar(C::kBarQDFull + s), (j >> 1) & 1, ac))) break;
+                const int s = j % C::kQStages;
+                if (!(ok = mbar_wait(bar(C::kBarQDFull + s), (j / C::kQStages) & 1, ac))) break;
                 tc_fence_after();
                 const uint32_t sQ = sb + C::kOffStage + s * C::kStageBytes;
                 const uint32_t sdO = sQ + C::kTileBytes;
@@ -368,7 +403,70 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
         __syncwarp();
-    } else if (warp >= 8) {
+    } else if (RES && warp == 14) {
+        // -------------------------------------- residual chunk loader
+        // Bias and incoming-gradient chunks by TMA (zero fill past N); a
+        // gradient chunk with no incoming gradient is only handed over.
+        if (lane == 0) {
+            bool ok = true;
+            int slot = 0, issued = 0, gi = 0;
+            uint32_t phase = 0;
+            for (int j = 0; j < n_items && ok; ++j) {
+                const int qi = item_qi(j), bhq = item_bhq(j);
+                for (int idx = 0; idx < res_per_item; ++idx, ++gi) {
+                    if (gi >= kResSlots) ok = mbar_wait(bar(C::kBarResFree + slot), phase ^ 1u, ac);
+                    if (!ok) break;
+                    const bool is_bias = idx < res_bias;
+                    const int c = is_bias ? idx : idx - res_bias;
+                    const uint32_t full = bar(C::kBarResFull + slot);
+                    const CUtensorMap *map = is_bias ? &tmBias : (p.has_gin ? &tmGin : nullptr);
+                    if (map) {
+                        mbar_arrive_expect_tx(full, kResChunkBytes);
+                        for (int bx = 0; bx < kTile / kResQ; ++bx)
+                            tma_load_3d(sb + C::kOffRes + slot * kResChunkBytes + bx * (kResQ * 128),
+                                        map, full, kt * kTile + bx * kResQ, qi * kTile + c * kResQ,
+                                        bhq);
+                    } else {
+                        mbar_arrive(full);
+                    }
+                    issued = gi + 1;
+                    if (++slot == kResSlots) { slot = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                for (int x = max(issued - kResSlots, 0); x < issued; ++x)
+                    drain_wait(bar(C::kBarResFull + x % C::kResRing),
+                               static_cast<uint32_t>(x / C::kResRing) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (RES && warp == 15) {
+        // ---------------------------------- outgoing logit-gradient storer
+        if (lane == 0) {
+            bool ok = true;
+            int slot = 0;
+            uint32_t phase = 0;
+            for (int j = 0; j < n_items && ok; ++j) {
+                const int qi = item_qi(j), bhq = item_bhq(j);
+                for (int idx = 0; idx < res_per_item; ++idx) {
+                    if (!(ok = mbar_wait(bar(C::kBarResDone + slot), phase, ac))) break;
+                    if (idx >= res_bias && p.has_gout) {
+                        const int c = idx - res_bias;
+                        for (int bx = 0; bx < kTile / kResQ; ++bx)
+                            tma_store_3d(&tmGout,
+                                         sb + C::kOffRes + slot * kResChunkBytes + bx * (kResQ * 128),
+                                         kt * kTile + bx * kResQ, qi * kTile + c * kResQ, bhq);
+                        tma_store_commit();
+                        tma_store_wait_read();
+                    }
+                    mbar_arrive(bar(C::kBarResFree + slot));
+                    if (++slot == kResSlots) { slot = 0; phase ^= 1u; }
+                }
+            }
+            tma_store_wait_read();
+        }
+        __syncwarp();
+    } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------ dQ drain warpgroup
         // dQ(j) is staged (fp32, 128-byte swizzled boxes of 32 columns) in the
         // Q/dO buffers of item j's stage -- exactly 128 x D x 4 bytes, free
@@ -378,7 +476,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int qr = threadIdx.x - 256;
         const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 8) * 32) << 16) + C::kColDP;
         for (int j = 0; j < n_items; ++j) {
-            const int s = j & 1;
+            const int s = j % C::kQStages;
             const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
             // All four drain warps leave together (they meet at a barrier below).
             if (named_bar_or(2, kTile, !got)) break;
@@ -433,12 +531,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t sDS = sb + C::kOffDS;
         const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
         const uint64_t sm2 = f2pack(p.scale, p.scale);
+        const uint64_t l2e2 = f2pack(kLog2e, kLog2e);
+        // Offsets of key row kr inside a residual chunk (four 32-key boxes,
+        // 128-byte rows of 32 fp32, 16-byte pieces swizzled by row % 8).
+        const uint32_t res_koff = (kr / kResQ) * (kResQ * 128) + (kr % 4) * 4;
+        const int res_kpiece = (kr % kResQ) / 4;
         bool ok = true;
         for (int j = 0; j < n_items; ++j) {
-            const int s = j & 1;
+            const int s = j % C::kQStages;
             // --- P^T(j) = 2^(S^T scale log2e - LSE log2e), bf16 into TMEM over S^T
             ok = mbar_wait_warp(bar(C::kBarSFull), j & 1, ac);
-            if (ok) ok = mbar_wait_warp(bar(C::kBarQDFull + s), (j >> 1) & 1, ac);
+            if (ok) ok = mbar_wait_warp(bar(C::kBarQDFull + s), (j / C::kQStages) & 1, ac);
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && (item_qi(j) == kt);
@@ -448,6 +551,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t s_lse = s_rows + s * kTile * 4 + w * 256;
             const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4 + w * 256;
             uint32_t pw[32];   // P^T of this warpgroup's 64 columns, bf16 pairs
+            // Residual chunks of this warpgroup: query columns 64w + 32h .. +31
+            // are chunk 2w + h of the bias and of the logit gradient.
+            uint32_t bslot[2] = {0u, 0u}, gslot[2] = {0u, 0u};
+            int bsi[2] = {0, 0}, gsi[2] = {0, 0};
+            if constexpr (RES) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int gb = j * res_per_item + 2 * w + h;
+                    const int gg = gb + res_bias;
+                    bsi[h] = gb % kResSlots;
+                    gsi[h] = gg % kResSlots;
+                    bslot[h] = sb + C::kOffRes + bsi[h] * kResChunkBytes + res_koff;
+                    gslot[h] = sb + C::kOffRes + gsi[h] * kResChunkBytes + res_koff;
+                    if (res_bias && ok)
+                        ok = mbar_wait_warp(bar(C::kBarResFull + bsi[h]),
+                                            static_cast<uint32_t>(gb / kResSlots) & 1u, ac);
+                }
+                if (!ok) break;
+            }
             {
                 uint32_t sr[64];
                 tmem_ld64(tS, sr);
@@ -458,8 +580,20 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     for (int u = 0; u < 4; u += 2) {
                         const float la = u == 0 ? l4.x : l4.z, lb = u == 0 ? l4.y : l4.w;
                         float t0, t1;
+                        uint64_t off2 = f2pack(-la, -lb);   // -LSE log2e
+                        if constexpr (RES) {
+                            if (res_bias) {   // + bias log2e, read transposed from the chunk
+                                const int rq = (c + u) % kResQ;
+                                const uint32_t ba = bslot[(c + u) / kResQ] + rq * 128;
+                                const float b0 = ld_shared_f32(
+                                    ba + (static_cast<uint32_t>(res_kpiece ^ (rq & 7)) << 4));
+                                const float b1 = ld_shared_f32(
+                                    ba + 128 + (static_cast<uint32_t>(res_kpiece ^ ((rq + 1) & 7)) << 4));
+                                off2 = ffma2(f2pack(b0, b1), l2e2, off2);
+                            }
+                        }
                         f2unpack(ffma2(f2pack(__uint_as_float(sr[c + u]), __uint_as_float(sr[c + u + 1])),
-                                       sc2, f2pack(-la, -lb)), t0, t1);
+                                       sc2, off2), t0, t1);
                         float p0 = ex2(t0), p1 = ex2(t1);
                         if (diag || wedge) {
                             // kept iff 0 <= query - key < W (no upper limit without a window)
@@ -473,6 +607,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
             }
             tmem_st32(tS, pw);   // columns 64w..64w+31, already read
+            if constexpr (RES) {
+                if (res_bias) {   // bias chunks read: hand them back
+                    mbar_arrive(bar(C::kBarResDone + bsi[0]));
+                    mbar_arrive(bar(C::kBarResDone + bsi[1]));
+                }
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(C::kBarPReady));
@@ -484,6 +624,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                if constexpr (RES) {
+                    if (res_grad && !mbar_wait_warp(bar(C::kBarResFull + gsi[h]),
+                                                    static_cast<uint32_t>(
+                                                        (j * res_per_item + res_bias + 2 * w + h) /
+                                                        kResSlots) & 1u,
+                                                    ac)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 uint32_t dr[32];
                 tmem_ld32(tDP + h * 32, dr);
 #pragma unroll
@@ -502,15 +652,47 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         const float2 pp = __bfloat1622float2(
                             *reinterpret_cast<const __nv_bfloat162 *>(&pw[(cc + u) >> 1]));
                         float d0, d1;
-                        f2unpack(fmul2(fmul2(f2pack(pp.x, pp.y), f2pack(e0, e1)), sm2), d0, d1);
-                        wv[u >> 1] = pack_bf16x2(d0, d1);
+                        if constexpr (RES) {
+                            // total logit gradient: P (dP - Delta) + incoming, 0 where masked
+                            f2unpack(fmul2(f2pack(pp.x, pp.y), f2pack(e0, e1)), d0, d1);
+                            const int rq = c + u;   // query row within chunk h
+                            const uint32_t ga0 = gslot[h] + rq * 128 +
+                                                 (static_cast<uint32_t>(res_kpiece ^ (rq & 7)) << 4);
+                            const uint32_t ga1 = gslot[h] + (rq + 1) * 128 +
+                                                 (static_cast<uint32_t>(res_kpiece ^ ((rq + 1) & 7)) << 4);
+                            if (res_grad && p.has_gin) {
+                                d0 += ld_shared_f32(ga0);
+                                d1 += ld_shared_f32(ga1);
+                            }
+                            if (diag || wedge) {
+                                const int dq0 = qoff + w * 64 + cc + u - kr;
+                                const int wl = wedge ? p.window : (1 << 30);
+                                d0 = (dq0 >= 0 && dq0 < wl) ? d0 : 0.f;
+                                d1 = (dq0 + 1 >= 0 && dq0 + 1 < wl) ? d1 : 0.f;
+                            }
+                            if (res_grad && p.has_gout) {
+                                st_shared_f32(ga0, d0);
+                                st_shared_f32(ga1, d1);
+                            }
+                            wv[u >> 1] = pack_bf16x2(d0 * p.scale, d1 * p.scale);
+                        } else {
+                            f2unpack(fmul2(fmul2(f2pack(pp.x, pp.y), f2pack(e0, e1)), sm2), d0, d1);
+                            wv[u >> 1] = pack_bf16x2(d0, d1);
+                        }
                     }
                     const int chunk = cc >> 3;     // 16-byte chunk within the 64-query atom
                     st_shared_v4(sDS + w * (kTile * 128) + kr * 128 +
                                      (static_cast<uint32_t>(chunk ^ (kr & 7)) << 4),
                                  wv[0], wv[1], wv[2], wv[3]);
                 }
+                if constexpr (RES) {
+                    if (res_grad) {   // chunk h done: written back for the storer
+                        if (p.has_gout) fence_proxy_async_smem();
+                        mbar_arrive(bar(C::kBarResDone + gsi[h]));
+                    }
+                }
             }
+            if (!ok) break;
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(C::kBarDSReady));
@@ -558,9 +740,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
+template <int D, bool RES>
+cudaError_t launch_main(const CUtensorMap (&m)[10], const BwdParams &prm, unsigned grid,
+                        bool causal, cudaStream_t stream) {
+    using C = BwdCfg<D, RES>;
+    auto kern = causal ? bwd_main_kernel<D, true, RES> : bwd_main_kernel<D, false, RES>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, bwd_threads<RES>(), C::kSmemBytes, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5],
+                                                              m[6], m[7], m[8], m[9], prm);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
-    using C = BwdCfg<D>;
     const long long BH = static_cast<long long>(pb.B) * pb.Hq;
     const long long BHkv = static_cast<long long>(pb.B) * pb.Hkv;
     const int n_tiles = pb.NP / kTile;
@@ -573,15 +767,28 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
 
     // 2. main kernel.
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-    if (!encode_bf16_rows(&tq, pb.q, D, pb.N, BH, kTile) ||
-        !encode_bf16_rows(&tk, pb.k, D, pb.N, BHkv, kTile) ||
-        !encode_bf16_rows(&tv, pb.v, D, pb.N, BHkv, kTile) ||
-        !encode_bf16_rows(&tdo, pb.dO, D, pb.N, BH, kTile) ||
-        !encode_bf16_rows(&tdk, pb.dk, D, pb.N, BHkv, kTile) ||
-        !encode_bf16_rows(&tdv, pb.dv, D, pb.N, BHkv, kTile) ||
-        !encode_f32_rows(&tdq, pb.dq_acc, D, pb.N, BH, kTile))
+    // maps: q, k, v, dO, dK, dV, dQ accumulator, bias, incoming and outgoing
+    // logit gradients (the last three: [B*Hq, N query rows, N keys] fp32 in
+    // 32 x 32 boxes; a map of the first given one stands in for absent ones).
+    CUtensorMap m[10];
+    if (!encode_bf16_rows(&m[0], pb.q, D, pb.N, BH, kTile) ||
+        !encode_bf16_rows(&m[1], pb.k, D, pb.N, BHkv, kTile) ||
+        !encode_bf16_rows(&m[2], pb.v, D, pb.N, BHkv, kTile) ||
+        !encode_bf16_rows(&m[3], pb.dO, D, pb.N, BH, kTile) ||
+        !encode_bf16_rows(&m[4], pb.dk, D, pb.N, BHkv, kTile) ||
+        !encode_bf16_rows(&m[5], pb.dv, D, pb.N, BHkv, kTile) ||
+        !encode_f32_rows(&m[6], pb.dq_acc, D, pb.N, BH, kTile))
         return cudaErrorInvalidValue;
+    const bool res = pb.bias || pb.grad_in || pb.grad_out;
+    m[7] = m[8] = m[9] = m[6];
+    if (res) {
+        const float *any = pb.bias ? pb.bias : (pb.grad_in ? pb.grad_in : pb.grad_out);
+        const float *src[3] = {pb.bias ? pb.bias : any, pb.grad_in ? pb.grad_in : any,
+                               pb.grad_out ? pb.grad_out : any};
+        for (int i = 0; i < 3; ++i)
+            if (!encode_f32_rows(&m[7 + i], src[i], pb.N, pb.N, BH, kResQ))
+                return cudaErrorInvalidValue;
+    }
     BwdParams prm;
     prm.lse2 = pb.lse2;
     prm.delta = pb.delta;
@@ -597,12 +804,12 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     prm.scale = pb.scale;
     prm.scale_log2 = pb.scale * kLog2e;
     prm.window = pb.causal ? pb.window : 0;
+    prm.has_bias = pb.bias != nullptr;
+    prm.has_gin = pb.grad_in != nullptr;
+    prm.has_gout = pb.grad_out != nullptr;
     const unsigned grid = static_cast<unsigned>(n_tiles * BHkv);
-    auto kern = pb.causal ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdq, prm);
-    e = cudaGetLastError();
+    e = res ? launch_main<D, true>(m, prm, grid, pb.causal, stream)
+            : launch_main<D, false>(m, prm, grid, pb.causal, stream);
     if (e != cudaSuccess) return e;
 
     // 3. fp32 dQ accumulator -> bf16 dQ.

@@ -31,6 +31,10 @@ struct BwdProblem {
     float scale;
     bool causal;
     int window;      // as in FwdProblem
+    // block residual (all null for the plain backward): fp32 [B,Hq,N,N]
+    const float *bias;       // the forward's logit bias
+    const float *grad_in;    // gradient arriving at this layer's logits
+    float *grad_out;         // total logit gradient (may alias grad_in)
     float *dq_acc;   // fp32 [B,Hq,N,D] inside the workspace
     float *lse2;     // fp32 [B*Hq, NP]: LSE * log2(e), +inf on padding rows
     float *delta;    // fp32 [B*Hq, NP]: rowsum(dO * O), 0 on padding rows
