@@ -235,7 +235,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::kBarSFull + s), 1);
-            mbar_init(bar(C::kBarPFull + s), kSoftThreads);
+            // the softmax threads' P, plus the producer's V_j (bytes)
+            mbar_init(bar(C::kBarPFull + s), kSoftThreads + 1);
         }
         mbar_init(bar(C::kBarODone), 1);
         mbar_init(bar(C::kBarOFinal), 1);
@@ -299,10 +300,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (j >= C::kVStages)
                     ok = mbar_wait(bar(C::kBarVEmpty + vs), ((j / C::kVStages) - 1) & 1, ac);
                 if (!ok) break;
-                mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTileBytes);
+                // V_j completes on P_j's barrier: the MMA issuer waits once for
+                // both.  The barrier's previous phase (tile j-2) must be over
+                // before it is armed for tile j: wait for PV_{j-2} (implied by
+                // the stage wait above when the V ring has at most 2 stages).
+                if (C::kVStages > 2 && j >= 2) {
+                    const int jp = j - 2;
+                    ok = mbar_wait(bar(C::kBarVEmpty + jp % C::kVStages),
+                                   (jp / C::kVStages) & 1, ac);
+                    if (!ok) break;
+                }
+                const uint32_t pv_bar = bar(C::kBarPFull + (j & 1));
+                mbar_arrive_expect_tx(pv_bar, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &tmV,
-                                bar(C::kBarVFull + vs), c * 64, (kv_lo + j) * kBlockN, bh_kv);
+                                pv_bar, c * 64, (kv_lo + j) * kBlockN, bh_kv);
                 v_issued = j + 1;
             }
             if (!ok) {
@@ -311,8 +323,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 drain_wait(bar(C::kBarQFull), 0);
                 for (int j = max(k_issued - C::kKStages, 0); j < k_issued; ++j)
                     drain_wait(bar(C::kBarKFull + j % C::kKStages), (j / C::kKStages) & 1);
-                for (int j = max(v_issued - C::kVStages, 0); j < v_issued; ++j)
-                    drain_wait(bar(C::kBarVFull + j % C::kVStages), (j / C::kVStages) & 1);
+                // (V loads complete on the P barriers, which may never fill
+                // after an abort: the drain then waits out its short limit.)
+                for (int j = max(v_issued - 2, 0); j < v_issued; ++j)
+                    drain_wait(bar(C::kBarPFull + (j & 1)), (j >> 1) & 1);
             }
         }
         __syncwarp();
@@ -328,7 +342,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 const int pb = i & 1;
                 if (!mbar_wait(bar(C::kBarPFull + pb), (i >> 1) & 1, ac)) return false;
                 const int vs = i % C::kVStages;
-                if (!mbar_wait(bar(C::kBarVFull + vs), (i / C::kVStages) & 1, ac)) return false;
                 tc_fence_after();
                 const uint32_t a_tmem = tmem + pb * kBlockN;   // P: bf16 pairs, cols 0..63
                 const uint32_t v_base = sb + C::kOffV + vs * C::kTileBytes;
