@@ -314,6 +314,9 @@ EXTRA_WORKLOADS = {
     # cache, grouped heads 32 : 8 (every K/V byte serves 4 query rows).
     "decode": dict(name="decode_B16_H32_KV8_N16384_D128", kind="decode", B=16, Hq=32, Hkv=8,
                    N=16384, D=128, causal=True),
+    "profile_chain_train_small": dict(name="residual_chain_train_4layers_B1_H10_KV2_N2048_D128",
+                                      kind="chain_train", layers=4, B=1, Hq=10, Hkv=2, N=2048,
+                                      D=128, causal=True),
     "profile_decode_small": dict(name="decode_B4_H32_KV8_N16384_D128", kind="decode", B=4,
                                  Hq=32, Hkv=8, N=16384, D=128, causal=True),
     # Causal sliding window of 4096 keys on the default step's shape.
@@ -583,7 +586,10 @@ def run_ours(args):
             ach = by / (avg * 1e-3) / 1e9
             kernels[lbl] = {"kernel": f"decode_split_kernel<{D}> + decode_merge_kernel",
                             "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                            "traffic": profiled_traffic(f"decode_split_kernel_{W['name']}",
+                                                        source_digest(DEC_SOURCES),
+                                                        B * Hkv * N),
                             "bytes_per_launch": by, "flops_per_launch": fl,
                             "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
                             "launches_timed": 2,
@@ -593,10 +599,16 @@ def run_ours(args):
             is_b = lbl.startswith("bwd")
             dg = source_digest(BWD_SOURCES if is_b else FWD_SOURCES)
             ach = by / (avg * 1e-3) / 1e9
+            ctag = f"causal_B{B}_H{Hq}_N{N}_D{D}"
             kernels[lbl] = {"kernel": ("bwd_main_kernel<%d,causal,residual> (+pre, dQ convert)" % D
                                        if is_b else f"fwd_kernel<{D},causal,bias/emit>"),
                             "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None,
+                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                            "traffic": (profiled_traffic(
+                                f"bwd_main_kernel_residual_chain_train_B{B}_H{Hq}_N{N}_D{D}", dg,
+                                units) if lbl in ("bwd1", "bwd2") else
+                                profiled_traffic(f"fwd_kernel_chain_{ctag}", dg, units)
+                                if lbl in ("fwd1", "fwd2") else None),
                             "bytes_per_launch": by, "flops_per_launch": fl,
                             "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
                             "launches_timed": 3 if is_b else 1, "source_digest": dg}
