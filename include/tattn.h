@@ -135,7 +135,9 @@ attn_status attn_fwd_window(const void *q, const void *k, const void *v, const f
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,Hq,N,D], plus two fp32 per-row arrays [B*Hq, NP]
  * (NP = N rounded up to a multiple of 128) holding LSE*log2(e) and
- * Delta_i = sum_d dO_id O_id; each region rounded up to 256 bytes.
+ * Delta_i = sum_d dO_id O_id, plus, with grouped heads (Hq > Hkv), fp32 dK
+ * and dV accumulators [B,Hkv,N,D] (used when a key tile's query heads are
+ * split over several thread blocks); each region rounded up to 256 bytes.
  * Returns 0 for an empty problem or invalid sizes.
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D);

@@ -94,7 +94,9 @@ def test_workspace_size(ta):
                                                                  + 2 * 16 * 16384 * 4)
     assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 64) == 768 + 2 * 512
     assert ta.attn_bwd_workspace_size(1, 1, 1, 5, 64) == 1280 + 2 * 512
-    assert ta.attn_bwd_workspace_size(2, 3, 1, 130, 64) == (6 * 130 * 64 * 4 + 2 * 6 * 256 * 4)
+    # grouped heads: + fp32 dK and dV accumulators [B,Hkv,N,D] (66560 bytes each here)
+    assert ta.attn_bwd_workspace_size(2, 3, 1, 130, 64) == (6 * 130 * 64 * 4 + 2 * 6 * 256 * 4
+                                                            + 2 * 66560)
     assert ta.attn_bwd_workspace_size(0, 1, 1, 3, 64) == 0
     # D = 80 and 96 rows: 320- and 384-byte fp32 rows
     assert ta.attn_bwd_workspace_size(1, 1, 1, 3, 80) == 1024 + 2 * 512

@@ -89,15 +89,18 @@ bool encode_f32_rows(CUtensorMap *map, const void *base, int D, int N, long long
     return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, N, heads, box_rows);
 }
 
-BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int D) {
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Hkv, int N, int D) {
     auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     const size_t rows = static_cast<size_t>(B) * Hq * N;
     const size_t prow = static_cast<size_t>(B) * Hq * (((static_cast<size_t>(N) + 127) / 128) * 128);
+    const size_t kvrows = Hq > Hkv ? static_cast<size_t>(B) * Hkv * N : 0;
     BwdWorkspace w;
     w.dq_acc = 0;
     w.lse2 = round256(rows * D * sizeof(float));
     w.delta = w.lse2 + round256(prow * sizeof(float));
-    w.total = w.delta + round256(prow * sizeof(float));
+    w.dk_acc = w.delta + round256(prow * sizeof(float));
+    w.dv_acc = w.dk_acc + round256(kvrows * D * sizeof(float));
+    w.total = w.dv_acc + round256(kvrows * D * sizeof(float));
     return w;
 }
 
@@ -185,7 +188,7 @@ attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
         const double elems = static_cast<double>(B) * Hq * static_cast<double>(N) * N;
         if (elems > 9.0e18) return ATTN_ERR_UNSUPPORTED;
     }
-    const BwdWorkspace wl = bwd_workspace_layout(B, Hq, N, D);
+    const BwdWorkspace wl = bwd_workspace_layout(B, Hq, Hkv, N, D);
     if (workspace_bytes < wl.total) return ATTN_ERR_INVALID;
     BwdProblem pb;
     pb.q = q;
@@ -212,6 +215,8 @@ attn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
     pb.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
     pb.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
     pb.delta = reinterpret_cast<float *>(ws + wl.delta);
+    pb.dk_acc = Hq > Hkv ? reinterpret_cast<float *>(ws + wl.dk_acc) : nullptr;
+    pb.dv_acc = Hq > Hkv ? reinterpret_cast<float *>(ws + wl.dv_acc) : nullptr;
     pb.NP = ((N + 127) / 128) * 128;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
@@ -298,7 +303,7 @@ attn_status attn_decode(const void *q, const void *k, const void *v, void *o, fl
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int D) {
     bool empty = false;
     if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
-    return bwd_workspace_layout(B, Hq, N, D).total;
+    return bwd_workspace_layout(B, Hq, Hkv, N, D).total;
 }
 
 attn_status attn_fwd(const void *q, const void *k, const void *v, const float *bias, void *o,

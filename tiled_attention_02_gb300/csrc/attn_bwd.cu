@@ -93,6 +93,15 @@ bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restr
     }
 }
 
+// ----------------------------------------------- accumulator zero fill
+
+__global__ void __launch_bounds__(256)
+bwd_zero_kernel(float4 *__restrict__ p, size_t n4) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // ------------------------------------------------------------ dQ convert
 
 __global__ void __launch_bounds__(256)
@@ -184,6 +193,9 @@ struct BwdParams {
     int window;   // causal sliding window W (key j kept for query i iff i - W < j), 0 = none
     // residual variant: which of the three fp32 [B,Hq,N,N] tensors are given
     int has_bias, has_gin, has_gout;
+    // blocks per (key tile, kv head): each takes group / hsplit query heads;
+    // with hsplit > 1, dK and dV are fp32 partial sums added into accumulators
+    int hsplit;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -237,8 +249,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int lane = threadIdx.x & 31;
 
     // Heaviest key tiles first under the causal mask (tile 0 sees every query tile).
-    const int kt = blockIdx.x / p.BHkv;
-    const int bh_kv = blockIdx.x % p.BHkv;
+    const int kt = blockIdx.x / (p.BHkv * p.hsplit);
+    const int bh_kv = (blockIdx.x % (p.BHkv * p.hsplit)) / p.hsplit;
+    const int hs = blockIdx.x % p.hsplit;          // which share of the group's query heads
+    const int hper = p.group / p.hsplit;           // query heads of this block
     const int b = bh_kv / p.Hkv, g = bh_kv % p.Hkv;
     // Query tiles q_lo .. q_lo + nq - 1 see this key tile: from the diagonal
     // (causal) to the tile holding query kt*128 + 127 + W - 1 (window).
@@ -247,14 +261,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                           ? min(p.n_tiles, (kt * kTile + kTile - 1 + p.window - 1) / kTile + 1)
                           : p.n_tiles;
     const int nq = q_end - q_lo;                  // query tiles per query head
-    const int n_items = p.group * nq;
+    const int n_items = hper * nq;
 
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     const AbortCtl ac{abort_flag, p.status};
     auto item_qi = [&](int j) { return q_lo + j % nq; };
-    auto item_bhq = [&](int j) { return b * p.Hq + g * p.group + j / nq; };
+    auto item_bhq = [&](int j) { return b * p.Hq + g * p.group + hs * hper + j / nq; };
     const uint32_t s_rows = sb + C::kOffRows;   // lse2[s][128] then delta[s][128]
     // Residual chunk sequence of item j: the bias chunks c = 0..3 (if a bias
     // is given), then the logit-gradient chunks c = 0..3 (if one flows in or
@@ -704,6 +718,52 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         named_bar_sync(3, 3 * kTile);   // the drain is done with the stage buffers
         const uint32_t stV = sb + C::kOffStage;                  // stage 0 Q buffer
         const uint32_t stK = sb + C::kOffStage + C::kTileBytes;  // stage 0 dO buffer
+        if (p.hsplit > 1) {
+            // Partial sums over this block's query heads: fp32 boxes of 32
+            // columns (as the dQ drain), added into the accumulators by TMA.
+            // With two stages dV and dK stage at once, else one after the other.
+            constexpr int kRounds = C::kQStages >= 2 ? 1 : 2;
+            for (int rd = 0; rd < kRounds; ++rd) {
+                const uint32_t dst = sb + C::kOffStage + (kRounds == 1 ? w * C::kStageBytes : 0);
+                if (ok && (kRounds == 1 || rd == w)) {
+                    tc_fence_after();
+                    const uint32_t tacc = tmem + lane_base + (w == 0 ? C::kColDV : C::kColDK);
+#pragma unroll
+                    for (int c = 0; c < C::kDQBoxes; c += 2) {
+                        uint32_t rr[64];
+                        const int nb = (c + 1 < C::kDQBoxes) ? 2 : 1;
+                        if (nb == 2) tmem_ld64(tacc + c * 32, rr);
+                        else tmem_ld32(tacc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {
+                            if (hb >= nb) break;
+                            const uint32_t box = dst + (c + hb) * (kTile * 128) + kr * 128;
+#pragma unroll
+                            for (int ch = 0; ch < 8; ++ch) {
+                                const int e = hb * 32 + ch * 4;
+                                st_shared_v4(box + (static_cast<uint32_t>(ch ^ (kr & 7)) << 4),
+                                             rr[e], rr[e + 1], rr[e + 2], rr[e + 3]);
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                named_bar_sync(1, 2 * kTile);
+                if (threadIdx.x == 0 && *abort_flag == 0) {
+                    for (int t2 = 0; t2 < 2; ++t2) {
+                        if (kRounds == 2 && t2 != rd) continue;
+                        const uint32_t src = sb + C::kOffStage + (kRounds == 1 ? t2 * C::kStageBytes : 0);
+                        for (int bx = 0; bx < C::kDQBoxes; ++bx)
+                            tma_reduce_add_3d(t2 == 0 ? &tmdV : &tmdK, src + bx * (kTile * 128),
+                                              bx * 32, kt * kTile, bh_kv);
+                    }
+                    tma_store_commit();
+                    tma_store_wait_read();
+                }
+                named_bar_sync(1, 2 * kTile);   // staging read before it is reused
+            }
+        } else {
         if (ok) {
             tc_fence_after();
             const uint32_t col = w == 0 ? C::kColDV : C::kColDK;
@@ -729,6 +789,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             tma_store_commit();
             tma_store_wait_read();
+        }
         }
     }
 
@@ -780,6 +841,28 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
         !encode_f32_rows(&m[6], pb.dq_acc, D, pb.N, BH, kTile))
         return cudaErrorInvalidValue;
     const bool res = pb.bias || pb.grad_in || pb.grad_out;
+    // Split a key tile's query heads over blocks when the grid would
+    // otherwise leave SMs idle or run a few long blocks (grouped heads only).
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    const int group = pb.Hq / pb.Hkv;
+    const int hsplit =
+        (group > 1 && pb.dk_acc && static_cast<long long>(n_tiles) * BHkv < 2LL * sms) ? group : 1;
+    if (hsplit > 1) {
+        // dK, dV through fp32 accumulators: zero them, map them in place of
+        // the bf16 outputs, convert at the end.
+        const size_t n_kv = static_cast<size_t>(BHkv) * pb.N * D;
+        const size_t span = static_cast<size_t>(pb.dv_acc - pb.dk_acc) + n_kv;
+        bwd_zero_kernel<<<static_cast<unsigned>(std::min<size_t>((span / 4 + 255) / 256, 152 * 8)),
+                          256, 0, stream>>>(reinterpret_cast<float4 *>(pb.dk_acc), span / 4);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (!encode_f32_rows(&m[4], pb.dk_acc, D, pb.N, BHkv, kTile) ||
+            !encode_f32_rows(&m[5], pb.dv_acc, D, pb.N, BHkv, kTile))
+            return cudaErrorInvalidValue;
+    }
     m[7] = m[8] = m[9] = m[6];
     if (res) {
         const float *any = pb.bias ? pb.bias : (pb.grad_in ? pb.grad_in : pb.grad_out);
@@ -807,15 +890,22 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     prm.has_bias = pb.bias != nullptr;
     prm.has_gin = pb.grad_in != nullptr;
     prm.has_gout = pb.grad_out != nullptr;
-    const unsigned grid = static_cast<unsigned>(n_tiles * BHkv);
+    prm.hsplit = hsplit;
+    const unsigned grid = static_cast<unsigned>(n_tiles * BHkv * hsplit);
     e = res ? launch_main<D, true>(m, prm, grid, pb.causal, stream)
             : launch_main<D, false>(m, prm, grid, pb.causal, stream);
     if (e != cudaSuccess) return e;
 
-    // 3. fp32 dQ accumulator -> bf16 dQ.
+    // 3. fp32 dQ accumulator -> bf16 dQ (and dK, dV when they were split).
     const size_t n8 = static_cast<size_t>(BH) * pb.N * D / 8;
     const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
     bwd_dq_kernel<<<blocks, 256, 0, stream>>>(pb.dq_acc, static_cast<__nv_bfloat16 *>(pb.dq), n8);
+    if (hsplit > 1) {
+        const size_t k8 = static_cast<size_t>(BHkv) * pb.N * D / 8;
+        const unsigned kb = static_cast<unsigned>(std::min<size_t>((k8 + 255) / 256, 152 * 16));
+        bwd_dq_kernel<<<kb, 256, 0, stream>>>(pb.dk_acc, static_cast<__nv_bfloat16 *>(pb.dk), k8);
+        bwd_dq_kernel<<<kb, 256, 0, stream>>>(pb.dv_acc, static_cast<__nv_bfloat16 *>(pb.dv), k8);
+    }
     return cudaGetLastError();
 }
 

@@ -38,6 +38,8 @@ struct BwdProblem {
     float *dq_acc;   // fp32 [B,Hq,N,D] inside the workspace
     float *lse2;     // fp32 [B*Hq, NP]: LSE * log2(e), +inf on padding rows
     float *delta;    // fp32 [B*Hq, NP]: rowsum(dO * O), 0 on padding rows
+    float *dk_acc;   // fp32 [B,Hkv,N,D] (grouped heads only): dK summed over query heads
+    float *dv_acc;   // fp32 [B,Hkv,N,D]  "   dV
     int NP;          // N rounded up to the 128-row tile
 };
 
@@ -59,9 +61,11 @@ int decode_max_splits(int N);
 // Byte offsets of the three workspace regions (each 256-byte aligned) and
 // the total size, for a validated shape.
 struct BwdWorkspace {
-    size_t dq_acc, lse2, delta, total;
+    size_t dq_acc, lse2, delta, dk_acc, dv_acc, total;
 };
-BwdWorkspace bwd_workspace_layout(int B, int Hq, int N, int D);
+// dk_acc / dv_acc exist only with grouped heads (Hq > Hkv), where the
+// backward may split a key tile's query heads over several blocks.
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Hkv, int N, int D);
 
 // Encodes a rank-3 bf16 tensor map over a [rows = N, cols = D] matrix per
 // head (dims {D, N, heads}) with a {64, box_rows, 1} box and 128-byte
