@@ -650,7 +650,7 @@ def run_ours(args):
             "data": "synthetic: q,k,v(,dO) ~ N(0,1) bf16, seeded",
             "config": dict(config_block(world, W),
                            step={"fwd_bwd": "forward + backward", "fwd": "forward",
-                                 "decode": "one decode step (split keys, then merge)",
+                                 "decode": "one decode step (stream-K over one block per SM, then merge)",
                                  "chain_train": "four chained layers forward, then backward "
                                                 "through the block (fp32 residual and gradient)",
                                  "chain": "four chained forward layers, fp32 residual in place"}[kind]),

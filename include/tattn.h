@@ -255,10 +255,11 @@ attn_status attn_bwd_noalloc(const void *q, const void *k, const void *v, const 
                              void *stream);
 
 /*
- * Bytes of device workspace attn_decode needs: per (batch, query head) and
- * per key split, an fp32 running max, row sum and D-column partial output
- * (at most min(64, ceil(N/128)) splits), each region rounded up to 256
- * bytes.  Returns 0 for an empty problem or invalid/unsupported sizes.
+ * Bytes of device workspace attn_decode needs: an fp32 running max, row sum
+ * and D-column partial output per query head and per segment (a run of one
+ * kv head's keys inside one thread block), for up to 512 + B*Hkv - 1
+ * segments of Hq/Hkv heads, each region rounded up to 256 bytes.  Returns 0
+ * for an empty problem or invalid/unsupported sizes.
  */
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int N, int D);
 
@@ -266,9 +267,10 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int N, int D);
  * Decode step (flash decode): one new query row per (batch, query head)
  * attends to an N-row key/value cache.  The query is at position N-1, so
  * the causal mask keeps all N keys; the result equals the last row of
- * attn_fwd with causal = 1 on the same cache.  The keys of each kv head are
- * split over several thread blocks and the partial softmax states are merged
- * with the online-softmax block-merge rule (kwkr.cn/news/592482, 2.2);
+ * attn_fwd with causal = 1 on the same cache.  The (kv head, 128-key) work
+ * is spread evenly over one thread block per SM; a kv head whose keys span
+ * several blocks has its partial softmax states merged with the
+ * online-softmax block-merge rule (kwkr.cn/news/592482, 2.2);
  * "FlashAttention原理与Triton实战" section 7 names flash decode as an
  * extension of the fused kernel.
  *

@@ -123,9 +123,12 @@ def test_window_entry_points_check_shapes_like_the_plain_ones(ta):
 
 
 def test_decode_workspace_size(ta):
-    # splits: min(64, ceil(N/128)); m and l [rows, splits], o [rows, splits, D]
-    assert ta.attn_decode_workspace_size(1, 1, 1, 100, 64) == 256 + 256 + 256
-    assert ta.attn_decode_workspace_size(2, 8, 2, 16384, 128) == 2 * (16 * 64 * 4) + 16 * 64 * 128 * 4
+    # slots = 512 + B*Hkv - 1 segments of G = Hq/Hkv heads: m and l [slots, G],
+    # o [slots, G, D], fp32, each region rounded up to 256 bytes
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert ta.attn_decode_workspace_size(1, 1, 1, 100, 64) == 2 * 512 * 4 + 512 * 64 * 4
+    assert ta.attn_decode_workspace_size(2, 8, 2, 16384, 128) == 2 * r256(515 * 4 * 4) + 515 * 4 * 128 * 4
+    assert ta.attn_decode_workspace_size(2, 8, 2, 100, 128) == ta.attn_decode_workspace_size(2, 8, 2, 16384, 128)
     assert ta.attn_decode_workspace_size(1, 32, 1, 1024, 64) == 0     # 32 query heads per kv head
     assert ta.attn_decode_workspace_size(1, 2, 2, 1024, 72) == 0
 

@@ -44,6 +44,9 @@ CASES = [
     (3, 6, 2, 777, 80),        # D = 80
     (2, 12, 4, 4096, 96),      # D = 96
     (1, 5, 1, 20000, 128),     # long cache: many splits
+    (2, 16, 2, 4096, 64),      # D = 64 with 8:1 groups over several splits
+    (40, 8, 8, 1000, 128),     # several kv heads per block, segments straddling blocks
+    (8, 32, 8, 300, 96),       # short caches: blocks of one or two stages
 ]
 
 

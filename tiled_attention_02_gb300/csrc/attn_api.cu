@@ -229,9 +229,11 @@ struct DecWorkspace {
     size_t m, l, o, total;
 };
 
-DecWorkspace decode_workspace_layout(int B, int Hq, int N, int D) {
+DecWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D) {
     auto round256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t parts = static_cast<size_t>(B) * Hq * decode_max_splits(N);
+    // One slot per (block, kv head) segment: at most blocks + kv heads - 1.
+    const size_t slots = static_cast<size_t>(kDecodeMaxBlocks) + static_cast<size_t>(B) * Hkv - 1;
+    const size_t parts = slots * static_cast<size_t>(Hq / Hkv);
     DecWorkspace w;
     w.m = 0;
     w.l = round256(parts * sizeof(float));
@@ -250,7 +252,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int N, int D) {
     bool empty = false;
     if (check_sizes(B, Hq, Hkv, N, D, 1.0f, &empty) != ATTN_OK || empty) return 0;
     if (Hq / Hkv > kDecodeMaxGroup) return 0;
-    return decode_workspace_layout(B, Hq, N, D).total;
+    return decode_workspace_layout(B, Hq, Hkv, D).total;
 }
 
 attn_status attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -264,18 +266,17 @@ attn_status attn_decode(const void *q, const void *k, const void *v, void *o, fl
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
         (lse && !aligned(lse, 4)) || !aligned(workspace, 256))
         return ATTN_ERR_INVALID;
-    const DecWorkspace wl = decode_workspace_layout(B, Hq, N, D);
+    const DecWorkspace wl = decode_workspace_layout(B, Hq, Hkv, D);
     if (workspace_bytes < wl.total) return ATTN_ERR_INVALID;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    // Split the keys so that about four blocks per SM run (one resident at a
-    // time), each over a whole number of 64-key stages.
-    const long long groups = static_cast<long long>(B) * Hkv;
-    long long s = (4LL * sms + groups - 1) / groups;
-    s = s < 1 ? 1 : (s > decode_max_splits(N) ? decode_max_splits(N) : s);
-    const int chunk = static_cast<int>(((N + s - 1) / s + 63) / 64 * 64);
+    // One persistent block per SM (each holds most of an SM's shared
+    // memory), never more blocks than 128-key stages.
+    const long long stages = decode_stages(B, Hkv, N);
+    long long grid = sms < kDecodeMaxBlocks ? sms : kDecodeMaxBlocks;
+    if (grid > stages) grid = stages;
     DecProblem pb;
     pb.q = q;
     pb.k = k;
@@ -288,8 +289,7 @@ attn_status attn_decode(const void *q, const void *k, const void *v, void *o, fl
     pb.N = N;
     pb.D = D;
     pb.scale = scale;
-    pb.chunk = chunk;
-    pb.splits = (N + chunk - 1) / chunk;
+    pb.grid = static_cast<int>(grid);
     char *ws = static_cast<char *>(workspace);
     pb.m_part = reinterpret_cast<float *>(ws + wl.m);
     pb.l_part = reinterpret_cast<float *>(ws + wl.l);

@@ -43,20 +43,24 @@ struct BwdProblem {
     int NP;          // N rounded up to the 128-row tile
 };
 
-// Validated decode problem: one query row per (batch, query head) against an
-// N-row key/value cache, keys split over `splits` CTAs of `chunk` keys.
+// Decode problem: one query row per (batch, query head) against an N-row
+// key/value cache, the (kv head, 128-key stage) work spread evenly over
+// `grid` persistent blocks.
 struct DecProblem {
     const void *q, *k, *v;   // q [B,Hq,D], k/v [B,Hkv,N,D] bf16
     void *o;                 // [B,Hq,D] bf16
     float *lse;              // [B,Hq] or null
     int B, Hq, Hkv, N, D;
     float scale;
-    int splits, chunk;
-    float *m_part, *l_part, *o_part;   // workspace: [B*Hq, splits] x2, [B*Hq, splits, D]
+    int grid;
+    // workspace: [slots, G] x2 and [slots, G, D] fp32, slots = grid + B*Hkv - 1
+    float *m_part, *l_part, *o_part;
 };
 
-// Largest split count the decode workspace is sized for.
-int decode_max_splits(int N);
+// Most blocks a decode launch uses (the workspace is sized for it).
+constexpr int kDecodeMaxBlocks = 512;
+// 128-key stages of a decode problem: B * Hkv * ceil(N / 128).
+long long decode_stages(int B, int Hkv, int N);
 
 // Byte offsets of the three workspace regions (each 256-byte aligned) and
 // the total size, for a validated shape.
