@@ -408,6 +408,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 mma_commit(bar(C::kBarDQFull));   // also: every MMA of item j has completed
                 mma_commit(bar(C::kBarDSFree));
+                // With the register drain (residual variant) the {Q, dO} stage
+                // is free now; otherwise the drain hands it back once its
+                // reductions have read the dQ staged there.
+                if constexpr (RES) mma_commit(bar(C::kBarQDEmpty + s));
             }
             if (ok) {
                 mma_commit(bar(C::kBarAccDone));
@@ -482,56 +486,102 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------ dQ drain warpgroup
-        // dQ(j) is staged (fp32, 128-byte swizzled boxes of 32 columns) in the
-        // Q/dO buffers of item j's stage -- exactly 128 x D x 4 bytes, free
-        // once item j's MMAs are done -- and added into the fp32 accumulator
-        // with TMA bulk reductions.  The stage is handed back to the producer
-        // only after the reductions have read it.
-        const int qr = threadIdx.x - 256;
-        const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 8) * 32) << 16) + C::kColDP;
-        for (int j = 0; j < n_items; ++j) {
-            const int s = j % C::kQStages;
-            const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
-            // All four drain warps leave together (they meet at a barrier below).
-            if (named_bar_or(2, kTile, !got)) break;
-            tc_fence_after();
-            const uint32_t stage = sb + C::kOffStage + s * C::kStageBytes;
+        if constexpr (RES) {
+            // dQ(j) goes from TMEM straight into the fp32 accumulator with vector
+            // reductions, so no shared memory holds it and the {Q, dO} stage (the
+            // only one in this variant) is released as soon as the item's MMAs
+            // are done (the MMA thread commits it).  The 16x256b load shape hands four consecutive threads one
+            // 32-byte piece of a query row, so each red.global.add.v2.f32 of a
+            // warp adds 8 whole sectors -- the same L2 work per byte as a TMA
+            // reduction.  Warp 8 + w drains query rows 32w .. 32w + 31 (its TMEM
+            // lanes) in two halves of 16; the TMEM columns are handed back after
+            // the second half's load, before its reductions are issued.
+            constexpr int kUnits = D / 8;
+            const int wq = warp - 8;
+            const int r_in = lane >> 2;          // row within a half (and + 8)
+            const int c_in = 2 * (lane & 3);     // first of the thread's two columns in a unit
+            for (int j = 0; j < n_items; ++j) {
+                const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
+                // All four drain warps leave together.
+                if (named_bar_or(2, kTile, !got)) break;
+                tc_fence_after();
+                const int qi = item_qi(j), bhq = item_bhq(j);
+                float *rows = p.dq_acc + (static_cast<size_t>(bhq) * p.N + qi * kTile) * D;
+                const int valid = p.N - qi * kTile;   // rows of this tile inside N
 #pragma unroll
-            for (int c = 0; c < C::kDQBoxes; c += 2) {
-                // Two 32-column boxes per 64-column load; a last odd box
-                // (D = 80, 96) takes a 32-column load, whose columns past D
-                // are clipped by the reduction.
-                constexpr int kPair = 2;
-                uint32_t rr[64];
-                const int nb = (c + 1 < C::kDQBoxes) ? kPair : 1;
-                if (nb == 2) tmem_ld64(tDQ + c * 32, rr);
-                else tmem_ld32(tDQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t v[4 * kUnits];
+                    const int r0 = 32 * wq + 16 * hf + r_in;
+                    tmem_ld_16x256b<kUnits>(
+                        tmem + (static_cast<uint32_t>(32 * wq + 16 * hf) << 16) + C::kColDP, v);
+                    if (hf == 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(C::kBarDQEmpty));   // TMEM columns of dQ are free
+                    }
 #pragma unroll
-                for (int hb = 0; hb < kPair; ++hb) {
-                    if (hb >= nb) break;
-                    const uint32_t box = stage + (c + hb) * (kTile * 128) + qr * 128;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const int e = hb * 32 + ch * 4;
-                        st_shared_v4(box + (static_cast<uint32_t>(ch ^ (qr & 7)) << 4), rr[e],
-                                     rr[e + 1], rr[e + 2], rr[e + 3]);
+                    for (int u = 0; u < kUnits; ++u) {
+                        if (r0 < valid)
+                            red_add_v2_f32(rows + static_cast<size_t>(r0) * D + 8 * u + c_in,
+                                           v[4 * u], v[4 * u + 1]);
+                        if (r0 + 8 < valid)
+                            red_add_v2_f32(rows + static_cast<size_t>(r0 + 8) * D + 8 * u + c_in,
+                                           v[4 * u + 2], v[4 * u + 3]);
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(C::kBarDQEmpty));          // TMEM columns of dQ are free
-            fence_proxy_async_smem();
-            named_bar_sync(2, kTile);
-            if (qr == 0) {
-                const int qi = item_qi(j), bhq = item_bhq(j);
-                for (int bx = 0; bx < C::kDQBoxes; ++bx)
-                    tma_reduce_add_3d(&tmDQ, stage + bx * (kTile * 128), bx * 32, qi * kTile, bhq);
-                tma_store_commit();
-                tma_store_wait_read();
-                mbar_arrive(bar(C::kBarQDEmpty + s));   // stage reusable by the producer
+        } else {
+            // dQ(j) is staged (fp32, 128-byte swizzled boxes of 32 columns) in the
+            // Q/dO buffers of item j's stage -- exactly 128 x D x 4 bytes, free
+            // once item j's MMAs are done -- and added into the fp32 accumulator
+            // with TMA bulk reductions.  The stage is handed back to the producer
+            // only after the reductions have read it.
+            const int qr = threadIdx.x - 256;
+            const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 8) * 32) << 16) + C::kColDP;
+            for (int j = 0; j < n_items; ++j) {
+                const int s = j % C::kQStages;
+                const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
+                // All four drain warps leave together (they meet at a barrier below).
+                if (named_bar_or(2, kTile, !got)) break;
+                tc_fence_after();
+                const uint32_t stage = sb + C::kOffStage + s * C::kStageBytes;
+#pragma unroll
+                for (int c = 0; c < C::kDQBoxes; c += 2) {
+                    // Two 32-column boxes per 64-column load; a last odd box
+                    // (D = 80, 96) takes a 32-column load, whose columns past D
+                    // are clipped by the reduction.
+                    constexpr int kPair = 2;
+                    uint32_t rr[64];
+                    const int nb = (c + 1 < C::kDQBoxes) ? kPair : 1;
+                    if (nb == 2) tmem_ld64(tDQ + c * 32, rr);
+                    else tmem_ld32(tDQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+#pragma unroll
+                    for (int hb = 0; hb < kPair; ++hb) {
+                        if (hb >= nb) break;
+                        const uint32_t box = stage + (c + hb) * (kTile * 128) + qr * 128;
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const int e = hb * 32 + ch * 4;
+                            st_shared_v4(box + (static_cast<uint32_t>(ch ^ (qr & 7)) << 4), rr[e],
+                                         rr[e + 1], rr[e + 2], rr[e + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(C::kBarDQEmpty));          // TMEM columns of dQ are free
+                fence_proxy_async_smem();
+                named_bar_sync(2, kTile);
+                if (qr == 0) {
+                    const int qi = item_qi(j), bhq = item_bhq(j);
+                    for (int bx = 0; bx < C::kDQBoxes; ++bx)
+                        tma_reduce_add_3d(&tmDQ, stage + bx * (kTile * 128), bx * 32, qi * kTile, bhq);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                    mbar_arrive(bar(C::kBarQDEmpty + s));   // stage reusable by the producer
+                }
             }
         }
-        // Hand stage 0 over to the dK/dV epilogue once its last reduction read it.
+        // Meet the P / dS warpgroups before their dK/dV epilogue (with the
+        // staged drain: once its last reduction has read stage 0).
         named_bar_sync(3, 3 * kTile);
     } else {
         // ---------------------------------------- two P / dS warpgroups
@@ -715,7 +765,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------ epilogue: dK, dV
         // Warpgroup 0 stores dV, warpgroup 1 stores dK (all D columns of each key row).
         if (ok) ok = mbar_wait_warp(bar(C::kBarAccDone), 0, ac);
-        named_bar_sync(3, 3 * kTile);   // the drain is done with the stage buffers
+        named_bar_sync(3, 3 * kTile);   // the drain warps are done
         const uint32_t stV = sb + C::kOffStage;                  // stage 0 Q buffer
         const uint32_t stK = sb + C::kOffStage + C::kTileBytes;  // stage 0 dO buffer
         if (p.hsplit > 1) {

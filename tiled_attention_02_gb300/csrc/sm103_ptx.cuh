@@ -419,6 +419,61 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
     }
 }
 
+// ---- 16x256b loads: 16 TMEM lanes x 8 columns per unit ----
+// Thread T receives, for unit u (columns 8u .. 8u+7 from taddr), the words
+// r[4u], r[4u+1] = lane (T/4), columns 8u + 2(T%4), +1 and r[4u+2], r[4u+3] =
+// lane (T/4) + 8, the same columns (lanes relative to taddr's lane field):
+// four consecutive threads hold one 32-byte piece of a row.
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TATTN_R8(0)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TATTN_R8(0), TATTN_R8(8)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TATTN_R8(0), TATTN_R8(8), TATTN_R8(16), TATTN_R8(24)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_16x256b_x16(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : TATTN_R8(0), TATTN_R8(8), TATTN_R8(16), TATTN_R8(24), TATTN_R8(32), TATTN_R8(40), TATTN_R8(48), TATTN_R8(56)
+        : "r"(taddr)
+        : "memory");
+}
+// U units (U a multiple of 2, at most 16) through the widest loads that fit.
+template <int U, int O = 0, int R>
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[R]) {
+    static_assert(U % 2 == 0 && 4 * (O / 4 + U) <= R, "unit count");
+    if constexpr (U >= 16) {
+        tmem_ld_16x256b_x16(taddr, *reinterpret_cast<uint32_t(*)[64]>(&r[O]));
+        tmem_ld_16x256b<U - 16, O + 64>(taddr + 128, r);
+    } else if constexpr (U >= 8) {
+        tmem_ld_16x256b_x8(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[O]));
+        tmem_ld_16x256b<U - 8, O + 32>(taddr + 64, r);
+    } else if constexpr (U >= 4) {
+        tmem_ld_16x256b_x4(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[O]));
+        tmem_ld_16x256b<U - 4, O + 16>(taddr + 32, r);
+    } else if constexpr (U >= 2) {
+        tmem_ld_16x256b_x2(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[O]));
+    }
+}
+
 #undef TATTN_R8
 #undef TATTN_W8
 
@@ -492,6 +547,11 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
         : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
         : "memory");
     return r != 0;
+}
+
+// Adds two consecutive fp32 values into global memory (no return value).
+__device__ __forceinline__ void red_add_v2_f32(float *addr, uint32_t a, uint32_t b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
