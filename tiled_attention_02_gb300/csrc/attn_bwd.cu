@@ -156,8 +156,11 @@ struct BwdCfg {
     static constexpr int kResRing = RES ? kResSlots : 1;
     static constexpr int kOffBar = kOffRes + kNumResSlots * kResChunkBytes;
     static constexpr int kBarKV = 0;
-    static constexpr int kBarQDFull = 1;     // 2
-    static constexpr int kBarQDEmpty = 3;    // 2
+    // Per stage: QFull / QEmpty cover Q and the LSE / Delta rows (and dO too
+    // in the one-stage residual variant); DOFull / DOEmpty cover dO (two-stage
+    // variant), whose buffer also stages part of dQ.
+    static constexpr int kBarQFull = 1;      // 2
+    static constexpr int kBarQEmpty = 3;     // 2
     static constexpr int kBarSFull = 5;
     static constexpr int kBarDPFull = 6;
     static constexpr int kBarPReady = 7;
@@ -167,7 +170,9 @@ struct BwdCfg {
     static constexpr int kBarDSFree = 11;
     static constexpr int kBarAccDone = 12;
     static constexpr int kBarDrain = 13;
-    static constexpr int kBarResFull = 14;                        // kNumResSlots each
+    static constexpr int kBarDOFull = 14;    // 2
+    static constexpr int kBarDOEmpty = 16;   // 2
+    static constexpr int kBarResFull = 18;                        // kNumResSlots each
     static constexpr int kBarResDone = kBarResFull + kNumResSlots;
     static constexpr int kBarResFree = kBarResDone + kNumResSlots;
     static constexpr int kNumBars = kBarResFree + kNumResSlots;
@@ -281,8 +286,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         *abort_flag = 0;
         mbar_init(bar(C::kBarKV), 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(C::kBarQDFull + s), 1);
-            mbar_init(bar(C::kBarQDEmpty + s), 1);
+            mbar_init(bar(C::kBarQFull + s), 1);
+            mbar_init(bar(C::kBarQEmpty + s), 1);    // the MMA thread, after the item's MMAs
+            mbar_init(bar(C::kBarDOFull + s), 1);
+            mbar_init(bar(C::kBarDOEmpty + s), 4);   // the four drain warps (staged drain)
         }
         for (int s = 0; s < C::kNumResSlots; ++s) {
             mbar_init(bar(C::kBarResFull + s), 1);
@@ -295,7 +302,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(C::kBarDSReady), 2 * kTile);
         mbar_init(bar(C::kBarDQFull), 1);
         mbar_init(bar(C::kBarDQEmpty), kTile);
-        mbar_init(bar(C::kBarDSFree), 1);
+        // dS buffer free: the MMA thread (dK, dQ read it) and, with the staged
+        // drain, the four drain warps (part of dQ is staged there).
+        mbar_init(bar(C::kBarDSFree), RES ? 1 : 5);
         mbar_init(bar(C::kBarAccDone), 1);
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
@@ -320,30 +329,42 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tma_load_3d(sb + C::kOffV + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64,
                             kt * kTile, bh_kv);
             }
-            int issued = 0;
+            int issued = 0, issued_do = 0;
             for (int j = 0; j < n_items; ++j) {
                 const int s = j % C::kQStages;
-                if (j >= C::kQStages)
-                    ok = mbar_wait(bar(C::kBarQDEmpty + s), ((j / C::kQStages) - 1) & 1, ac);
-                if (!ok) break;
+                const uint32_t ph = ((j / C::kQStages) - 1) & 1;
+                if (j >= C::kQStages && !(ok = mbar_wait(bar(C::kBarQEmpty + s), ph, ac))) break;
                 const int qi = item_qi(j), bhq = item_bhq(j);
-                const uint32_t fb = bar(C::kBarQDFull + s);
-                mbar_arrive_expect_tx(fb, 2 * C::kTileBytes + 2 * kTile * 4);
+                const uint32_t fb = bar(C::kBarQFull + s);
+                // Q and the rows (and dO with one stage) on QFull, dO on DOFull
+                mbar_arrive_expect_tx(fb, (RES ? 2 : 1) * C::kTileBytes + 2 * kTile * 4);
                 const uint32_t st = sb + C::kOffStage + s * C::kStageBytes;
-                for (int c = 0; c < C::kChunks; ++c) {
+                for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(st + c * C::kChunkBytes, &tmQ, fb, c * 64, qi * kTile, bhq);
-                    tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tmdO, fb, c * 64,
-                                qi * kTile, bhq);
-                }
                 const size_t prow = static_cast<size_t>(bhq) * p.NP + qi * kTile;
                 bulk_load(s_rows + s * kTile * 4, p.lse2 + prow, kTile * 4, fb);
                 bulk_load(s_rows + (2 + s) * kTile * 4, p.delta + prow, kTile * 4, fb);
+                if constexpr (!RES) {
+                    issued = j + 1;
+                    if (j >= C::kQStages && !(ok = mbar_wait(bar(C::kBarDOEmpty + s), ph, ac)))
+                        break;
+                }
+                const uint32_t db = RES ? fb : bar(C::kBarDOFull + s);
+                if constexpr (!RES) mbar_arrive_expect_tx(db, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tmdO, db, c * 64,
+                                qi * kTile, bhq);
                 issued = j + 1;
+                issued_do = j + 1;
             }
             if (!ok) {
                 drain_wait(bar(C::kBarKV), 0);
                 for (int j = max(issued - C::kQStages, 0); j < issued; ++j)
-                    drain_wait(bar(C::kBarQDFull + j % C::kQStages), (j / C::kQStages) & 1);
+                    drain_wait(bar(C::kBarQFull + j % C::kQStages), (j / C::kQStages) & 1);
+                if constexpr (!RES) {
+                    for (int j = max(issued_do - C::kQStages, 0); j < issued_do; ++j)
+                        drain_wait(bar(C::kBarDOFull + j % C::kQStages), (j / C::kQStages) & 1);
+                }
             }
         }
         __syncwarp();
@@ -353,65 +374,119 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             constexpr uint32_t kIdS = idesc_bf16_f32(kTile, kTile, false, false);
             constexpr uint32_t kIdAcc = idesc_bf16_f32(kTile, D, false, true);   // dV, dK
             constexpr uint32_t kIdDQ = idesc_bf16_f32(kTile, D, true, true);     // dQ
-            bool ok = mbar_wait(bar(C::kBarKV), 0, ac);
-            for (int j = 0; j < n_items && ok; ++j) {
-                // Order per query tile j:
-                //   S^T(j)  dP^T(j)  [P_ready] dV(j)  [dS_ready] dK(j)  dQ(j)
-                // P is computed while dP^T runs and dS while dV runs.
-                const int s = j % C::kQStages;
-                if (!(ok = mbar_wait(bar(C::kBarQDFull + s), (j / C::kQStages) & 1, ac))) break;
+            const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV, sDS = sb + C::kOffDS;
+            auto stage_of = [&](int j) -> uint32_t {
+                return sb + C::kOffStage + (j % C::kQStages) * C::kStageBytes;
+            };
+            auto wait_stage = [&](int j) -> bool {   // Q (and dO with one stage)
+                if (!mbar_wait(bar(C::kBarQFull + j % C::kQStages), (j / C::kQStages) & 1, ac))
+                    return false;
                 tc_fence_after();
-                const uint32_t sQ = sb + C::kOffStage + s * C::kStageBytes;
-                const uint32_t sdO = sQ + C::kTileBytes;
-                const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV, sDS = sb + C::kOffDS;
+                return true;
+            };
+            auto wait_do = [&](int j) -> bool {
+                if (!mbar_wait(bar(C::kBarDOFull + j % C::kQStages), (j / C::kQStages) & 1, ac))
+                    return false;
+                tc_fence_after();
+                return true;
+            };
+            auto wait_on = [&](int b, int phase) -> bool {
+                if (!mbar_wait(bar(b), phase & 1, ac)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto issue_st = [&](int j) {   // S^T = K Q^T (over P^T(j-1), read by dV(j-1))
+                const uint32_t sQ = stage_of(j);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q^T (over P^T(j-1), read by dV(j-1))
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024),
                            sdesc_sw128(sQ + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::kBarSFull));
-                // dP^T overwrites dQ(j-1): the drain must have read it.
-                if (j > 0 && !(ok = mbar_wait(bar(C::kBarDQEmpty), (j - 1) & 1, ac))) break;
-                tc_fence_after();
+            };
+            auto issue_dpt = [&](int j) {   // dP^T = V dO^T (over dQ(j-1), drained)
+                const uint32_t sdO = stage_of(j) + C::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {   // dP^T = V dO^T
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024),
                            sdesc_sw128(sdO + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::kBarDPFull));
-                if (!(ok = mbar_wait(bar(C::kBarPReady), j & 1, ac))) break;
-                tc_fence_after();
+            };
+            auto issue_dv = [&](int j) {   // dV += P^T dO  (A in TMEM)
+                const uint32_t sdO = stage_of(j) + C::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {   // dV += P^T dO  (A in TMEM)
+                for (int kk = 0; kk < kTile / 16; ++kk) {
                     // P^T of query columns 64w..64w+63 sits in TMEM columns
                     // 64w..64w+31 (over warpgroup w's own, already read, S^T).
                     mma_ts(tmem + C::kColDV, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                            sdesc_sw128(sdO + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (!(ok = mbar_wait(bar(C::kBarDSReady), j & 1, ac))) break;
-                tc_fence_after();
+            };
+            auto issue_dk_dq = [&](int j) {   // dK += dS^T Q, then dQ = dS K (over dP^T(j), read)
+                const uint32_t sQ = stage_of(j);
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {   // dK += dS^T Q
+                for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + off, 16, 1024),
                            sdesc_sw128(sQ + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {   // dQ = dS K (both MN-major)
+                for (int kk = 0; kk < kTile / 16; ++kk) {   // both operands MN-major
                     mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + kk * 2048, C::kChunkBytes, 1024),
                            sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), kIdDQ,
                            kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::kBarDQFull));   // also: every MMA of item j has completed
                 mma_commit(bar(C::kBarDSFree));
-                // With the register drain (residual variant) the {Q, dO} stage
-                // is free now; otherwise the drain hands it back once its
-                // reductions have read the dQ staged there.
-                if constexpr (RES) mma_commit(bar(C::kBarQDEmpty + s));
+                // Q (and, with one stage, dO) of the item are free now; with two
+                // stages the drain hands dO's buffer back once its reductions
+                // have read the part of dQ staged there.
+                mma_commit(bar(C::kBarQEmpty + j % C::kQStages));
+            };
+            bool ok = mbar_wait(bar(C::kBarKV), 0, ac);
+            if constexpr (RES) {
+                // One {Q, dO} stage: per query tile j,
+                //   S^T(j)  dP^T(j)  [P ready] dV(j)  [dS ready] dK(j) dQ(j).
+                // P is computed while dP^T runs and dS while dV runs.
+                for (int j = 0; j < n_items && ok; ++j) {
+                    if (!(ok = wait_stage(j))) break;
+                    issue_st(j);
+                    if (j > 0 && !(ok = wait_on(C::kBarDQEmpty, j - 1))) break;
+                    issue_dpt(j);
+                    if (!(ok = wait_on(C::kBarPReady, j))) break;
+                    issue_dv(j);
+                    if (!(ok = wait_on(C::kBarDSReady, j))) break;
+                    issue_dk_dq(j);
+                }
+            } else {
+                // Two stages, software-pipelined over query tiles:
+                //   [P ready(j)] dV(j)  S^T(j+1)  [dS ready(j)] dK(j) dQ(j)
+                //   [dQ(j) drained] dP^T(j+1)
+                // so the P phase of tile j+1 runs while dK(j) and dQ(j) do.
+                if (ok && n_items > 0 && (ok = wait_stage(0))) {
+                    issue_st(0);
+                    if ((ok = wait_do(0))) issue_dpt(0);
+                }
+                for (int j = 0; j < n_items && ok; ++j) {
+                    if (!(ok = wait_on(C::kBarPReady, j))) break;
+                    issue_dv(j);
+                    if (j + 1 < n_items) {
+                        if (!(ok = wait_stage(j + 1))) break;
+                        issue_st(j + 1);
+                    }
+                    if (!(ok = wait_on(C::kBarDSReady, j))) break;
+                    issue_dk_dq(j);
+                    if (j + 1 < n_items) {
+                        if (!(ok = wait_on(C::kBarDQEmpty, j))) break;
+                        if (!(ok = wait_do(j + 1))) break;
+                        issue_dpt(j + 1);
+                    }
+                }
             }
             if (ok) {
                 mma_commit(bar(C::kBarAccDone));
@@ -530,20 +605,33 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
             }
         } else {
-            // dQ(j) is staged (fp32, 128-byte swizzled boxes of 32 columns) in the
-            // Q/dO buffers of item j's stage -- exactly 128 x D x 4 bytes, free
-            // once item j's MMAs are done -- and added into the fp32 accumulator
-            // with TMA bulk reductions.  The stage is handed back to the producer
-            // only after the reductions have read it.
+            // dQ(j) is staged as fp32, 128-byte swizzled boxes of 32 columns --
+            // boxes 0 and 1 in the dS buffer, the rest in item j's dO buffer,
+            // both free once item j's MMAs are done (Q's buffer is not used, so
+            // the next Q tile can load at once) -- and added into the fp32
+            // accumulator with TMA bulk reductions.  Each warp stages its own
+            // 32 query rows and reduces them with 32-row boxes, so the warps
+            // never wait on one another.  The dS buffer is handed back first
+            // (the P / dS warpgroups write the next dS there), then the dO
+            // buffer (the producer loads a later dO there).  The TMEM columns
+            // go back right after the last TMEM load (the next dP^T waits on
+            // them).
+            constexpr int kDsBoxes = C::kDQBoxes < 2 ? C::kDQBoxes : 2;
             const int qr = threadIdx.x - 256;
-            const uint32_t tDQ = tmem + (static_cast<uint32_t>((warp - 8) * 32) << 16) + C::kColDP;
+            const int wq = warp - 8;
+            const uint32_t tDQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDP;
+            const uint32_t sDS = sb + C::kOffDS;
             for (int j = 0; j < n_items; ++j) {
                 const int s = j % C::kQStages;
                 const bool got = mbar_wait_warp(bar(C::kBarDQFull), j & 1, ac);
-                // All four drain warps leave together (they meet at a barrier below).
+                // All four drain warps leave together.
                 if (named_bar_or(2, kTile, !got)) break;
                 tc_fence_after();
-                const uint32_t stage = sb + C::kOffStage + s * C::kStageBytes;
+                const uint32_t sDO = sb + C::kOffStage + s * C::kStageBytes + C::kTileBytes;
+                auto box_at = [&](int bx) -> uint32_t {
+                    return bx < kDsBoxes ? sDS + bx * (kTile * 128)
+                                         : sDO + (bx - kDsBoxes) * (kTile * 128);
+                };
 #pragma unroll
                 for (int c = 0; c < C::kDQBoxes; c += 2) {
                     // Two 32-column boxes per 64-column load; a last odd box
@@ -554,10 +642,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int nb = (c + 1 < C::kDQBoxes) ? kPair : 1;
                     if (nb == 2) tmem_ld64(tDQ + c * 32, rr);
                     else tmem_ld32(tDQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                    if (c + 2 >= C::kDQBoxes) {
+                        tc_fence_before();
+                        mbar_arrive(bar(C::kBarDQEmpty));   // TMEM columns of dQ are free
+                    }
 #pragma unroll
                     for (int hb = 0; hb < kPair; ++hb) {
                         if (hb >= nb) break;
-                        const uint32_t box = stage + (c + hb) * (kTile * 128) + qr * 128;
+                        const uint32_t box = box_at(c + hb) + qr * 128;
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
                             const int e = hb * 32 + ch * 4;
@@ -565,19 +657,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                          rr[e + 1], rr[e + 2], rr[e + 3]);
                         }
                     }
+                    // Boxes 0 and 1 (the dS buffer) are reduced first, while
+                    // the rest is loaded and staged; each box group is one
+                    // bulk group of this warp's lane 0.
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int row0 = item_qi(j) * kTile + wq * 32;
+                        if (row0 < p.N) {   // (rows past N are clipped by the reduction)
+                            for (int bx = c; bx < c + nb; ++bx)
+                                tma_reduce_add_3d(&tmDQ, box_at(bx) + wq * (32 * 128), bx * 32,
+                                                  row0, item_bhq(j));
+                        }
+                        tma_store_commit();
+                    }
                 }
-                tc_fence_before();
-                mbar_arrive(bar(C::kBarDQEmpty));          // TMEM columns of dQ are free
-                fence_proxy_async_smem();
-                named_bar_sync(2, kTile);
-                if (qr == 0) {
-                    const int qi = item_qi(j), bhq = item_bhq(j);
-                    for (int bx = 0; bx < C::kDQBoxes; ++bx)
-                        tma_reduce_add_3d(&tmDQ, stage + bx * (kTile * 128), bx * 32, qi * kTile, bhq);
-                    tma_store_commit();
+                if (lane == 0) {
+                    if constexpr (C::kDQBoxes <= 2) tma_store_commit();   // (no second group)
+                    tma_store_wait_read_n<1>();
+                    mbar_arrive(bar(C::kBarDSFree));          // this warp's dS-buffer part is read
                     tma_store_wait_read();
-                    mbar_arrive(bar(C::kBarQDEmpty + s));   // stage reusable by the producer
+                    mbar_arrive(bar(C::kBarDOEmpty + s));     // and its dO-buffer part
                 }
+                __syncwarp();
             }
         }
         // Meet the P / dS warpgroups before their dK/dV epilogue (with the
@@ -605,7 +707,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int s = j % C::kQStages;
             // --- P^T(j) = 2^(S^T scale log2e - LSE log2e), bf16 into TMEM over S^T
             ok = mbar_wait_warp(bar(C::kBarSFull), j & 1, ac);
-            if (ok) ok = mbar_wait_warp(bar(C::kBarQDFull + s), (j / C::kQStages) & 1, ac);
+            if (ok) ok = mbar_wait_warp(bar(C::kBarQFull + s), (j / C::kQStages) & 1, ac);
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && (item_qi(j) == kt);
@@ -888,7 +990,7 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
         !encode_bf16_rows(&m[3], pb.dO, D, pb.N, BH, kTile) ||
         !encode_bf16_rows(&m[4], pb.dk, D, pb.N, BHkv, kTile) ||
         !encode_bf16_rows(&m[5], pb.dv, D, pb.N, BHkv, kTile) ||
-        !encode_f32_rows(&m[6], pb.dq_acc, D, pb.N, BH, kTile))
+        !encode_f32_rows(&m[6], pb.dq_acc, D, pb.N, BH, 32))   // one drain warp's 32 rows
         return cudaErrorInvalidValue;
     const bool res = pb.bias || pb.grad_in || pb.grad_out;
     // Split a key tile's query heads over blocks when the grid would
