@@ -73,9 +73,16 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpLoader = 10;       // staged residual only
 constexpr int kWarpStorer = 11;       // staged residual only
+constexpr int kWarpOStore = 10;       // persistent plain forward: output tile storer
+
+// The plain forward (no residual) runs persistent blocks, one per SM, each
+// walking a list of (query tile, head) items; the residual variants take one
+// item per block.
+template <int EXT>
+constexpr bool fwd_persistent() { return EXT == 0; }
 
 template <int EXT>
-constexpr int fwd_threads() { return EXT == 2 ? 384 : 320; }
+constexpr int fwd_threads() { return EXT == 2 ? 384 : (EXT == 0 ? 352 : 320); }
 
 template <int D, int EXT>
 struct FwdCfg {
@@ -93,8 +100,11 @@ struct FwdCfg {
     // needed a whole softmax after its load is issued, so one V stage holds).
     static constexpr int kKStages = (D == 64) ? (EXT == 2 ? 2 : 3) : (EXT == 2 ? 1 : 2);
     static constexpr int kVStages = kKStages;
+    // Two Q buffers in the persistent variant: the next item's Q loads while
+    // this item's output is staged in (and stored from) its own Q buffer.
+    static constexpr int kQBufs = fwd_persistent<EXT>() ? 2 : 1;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kOffK = kOffQ + kQBufs * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kOffRes = kOffV + kVStages * kTileBytes;
     static constexpr int kRedBytes = 2 * 2 * kBlockM * 4;   // row-max exchange, 2 buffers
@@ -103,8 +113,10 @@ struct FwdCfg {
     static constexpr int kResRing = kResSlots > 0 ? kResSlots : 1;
     static constexpr int kOffBar = kOffRes + kResSlots * kResChunkBytes;
     // barrier indices
-    static constexpr int kBarQFull = 0;
-    static constexpr int kBarKFull = 1;
+    static constexpr int kBarQFull = 0;                       // 2 (per Q buffer)
+    static constexpr int kBarQEmpty = 2;                      // 2
+    static constexpr int kBarOStaged = 4;                     // 2: output tile staged in that Q buffer
+    static constexpr int kBarKFull = 6;
     static constexpr int kBarKEmpty = kBarKFull + kKStages;
     static constexpr int kBarVFull = kBarKEmpty + kKStages;
     static constexpr int kBarVEmpty = kBarVFull + kVStages;
@@ -204,18 +216,47 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Heaviest causal tiles first: block 0 gets the last query tile.
-    const int blk = blockIdx.x;
-    const int qt = CAUSAL ? (p.n_qtiles - 1 - blk / p.BH) : (blk / p.BH);
-    const int bh = blk % p.BH;
-    const int bh_kv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
     const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
-    // Key tiles kv_lo .. kv_lo + n_kv - 1: the causal mask ends them at the
-    // diagonal tile, a sliding window starts them at the tile holding key
-    // row_lo - W + 1 (the first key the tile's first row keeps).
-    const int row_lo = qt * kBlockM;
-    const int kv_lo = (CAUSAL && p.window > 0) ? max(0, row_lo - p.window + 1) / kBlockN : 0;
-    const int n_kv = (CAUSAL ? min(qt + 1, n_ktiles) : n_ktiles) - kv_lo;
+    const int n_items = p.n_qtiles * p.BH;
+    // This block's items (query tile, head): rounds of gridDim.x items, every
+    // other round in reverse block order, so that with the heaviest causal
+    // tiles first the blocks' totals stay balanced.  Round 0 only, unless the
+    // kernel is persistent (grid smaller than the item count).
+    auto item_at = [&](int rnd) -> int {
+        const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+        const int base = rnd * G;
+        if (base >= n_items) return -1;
+        const int k = base + ((rnd & 1) ? G - 1 - b : b);
+        return k < n_items ? k : -1;
+    };
+    struct Item {
+        int qt, bh, bh_kv, row_lo, kv_lo, n_kv;
+    };
+    auto decode = [&](int k) -> Item {
+        Item it;
+        // Causal: heaviest tiles first (item 0 is the last query tile of
+        // head 0), heads fastest.  Otherwise every item weighs the same, and
+        // query tiles go fastest so that the blocks running at once share a
+        // few heads' K/V in L2 instead of each streaming its own from HBM.
+        if (CAUSAL) {
+            it.qt = p.n_qtiles - 1 - k / p.BH;
+            it.bh = k % p.BH;
+        } else {
+            it.qt = k % p.n_qtiles;
+            it.bh = k / p.n_qtiles;
+        }
+        it.bh_kv = (it.bh / p.Hq) * p.Hkv + (it.bh % p.Hq) / p.group;
+        // Key tiles kv_lo .. kv_lo + n_kv - 1: the causal mask ends them at
+        // the diagonal tile, a sliding window starts them at the tile holding
+        // key row_lo - W + 1 (the first key the tile's first row keeps).
+        it.row_lo = it.qt * kBlockM;
+        it.kv_lo = (CAUSAL && p.window > 0) ? max(0, it.row_lo - p.window + 1) / kBlockN : 0;
+        it.n_kv = (CAUSAL ? min(it.qt + 1, n_ktiles) : n_ktiles) - it.kv_lo;
+        return it;
+    };
+    // The item of a one-item block (the residual variants' chunk roles).
+    const Item one = decode(max(item_at(0), 0));
+    const int qt = one.qt, bh = one.bh, kv_lo = one.kv_lo, n_kv = one.n_kv;
 
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -224,7 +265,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        mbar_init(bar(C::kBarQFull), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(C::kBarQFull + s), 1);
+            mbar_init(bar(C::kBarQEmpty + s), 1);   // the output storer
+            // One per buffer: an item's output can only be staged once the
+            // item two back has been stored, so the phases cannot run ahead.
+            mbar_init(bar(C::kBarOStaged + s), kSoftThreads);
+        }
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
             mbar_init(bar(C::kBarKEmpty + s), 1);
@@ -269,64 +316,99 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
     if (warp == kWarpProducer) {
         // ------------------------------------------------------ TMA producer
+        // Per item its Q tile (into Q buffer n_q % kQBufs, issued when the K
+        // cursor enters the item), then K and V per key tile.  K runs one tile
+        // ahead of V: K_{t+1} only waits for S_{t+1-KStages} to finish with its
+        // stage, while V_t waits for PV_{t-VStages}, which needs the softmax of
+        // that tile; issuing K first keeps the next S MMA from queueing behind
+        // a V wait.  The tile counters run on across items, so the rings and
+        // their barriers continue from one item to the next.
         if (lane == 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(bar(C::kBarQFull), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(sb + C::kOffQ + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull), c * 64,
-                            qt * kBlockM, bh);
-            // K runs one tile ahead of V: K_{j+1} only waits for S_{j+1-KStages}
-            // to finish with its stage, while V_j waits for PV_{j-VStages},
-            // which needs the softmax of that tile; issuing K first keeps the
-            // next S MMA from queueing behind a V wait.
-            int k_issued = 0, v_issued = 0;
-            auto load_k = [&](int j) -> bool {
-                const int ks = j % C::kKStages;
-                if (j >= C::kKStages &&
-                    !mbar_wait(bar(C::kBarKEmpty + ks), ((j / C::kKStages) - 1) & 1, ac))
+            int n_q = 0, k_issued = 0, v_issued = 0;
+            int kr = 0, kj = 0, vr = 0, vj = 0;   // K / V cursors: round, tile of the item
+            Item ki = decode(item_at(0)), vi = ki;
+            bool k_done = false, v_done = false;
+            auto advance = [&](int &rr, int &jj, Item &itm, bool &done) {
+                if (++jj == itm.n_kv) {
+                    jj = 0;
+                    const int k = item_at(++rr);
+                    if (k < 0) done = true;
+                    else itm = decode(k);
+                }
+            };
+            auto load_q = [&](const Item &itm) -> bool {
+                const int qb = n_q % C::kQBufs;
+                // The buffer's previous item must have stored its output.
+                if (n_q >= C::kQBufs &&
+                    !mbar_wait(bar(C::kBarQEmpty + qb), ((n_q / C::kQBufs) - 1) & 1, ac))
+                    return false;
+                mbar_arrive_expect_tx(bar(C::kBarQFull + qb), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sb + C::kOffQ + qb * C::kTileBytes + c * C::kChunkBytes, &tmQ,
+                                bar(C::kBarQFull + qb), c * 64, itm.row_lo, itm.bh);
+                ++n_q;
+                return true;
+            };
+            auto load_k = [&]() -> bool {
+                if (kj == 0 && !load_q(ki)) return false;
+                const int t = k_issued, ks = t % C::kKStages;
+                if (t >= C::kKStages &&
+                    !mbar_wait(bar(C::kBarKEmpty + ks), ((t / C::kKStages) - 1) & 1, ac))
                     return false;
                 mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &tmK,
-                                bar(C::kBarKFull + ks), c * 64, (kv_lo + j) * kBlockN, bh_kv);
-                k_issued = j + 1;
+                                bar(C::kBarKFull + ks), c * 64, (ki.kv_lo + kj) * kBlockN,
+                                ki.bh_kv);
+                k_issued = t + 1;
+                advance(kr, kj, ki, k_done);
                 return true;
             };
-            ok = load_k(0);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                if (j + 1 < n_kv) ok = load_k(j + 1);
-                if (!ok) break;
-                const int vs = j % C::kVStages;
-                if (j >= C::kVStages)
-                    ok = mbar_wait(bar(C::kBarVEmpty + vs), ((j / C::kVStages) - 1) & 1, ac);
-                if (!ok) break;
-                // V_j completes on P_j's barrier: the MMA issuer waits once for
-                // both.  The barrier's previous phase (tile j-2) must be over
-                // before it is armed for tile j: wait for PV_{j-2} (implied by
+            auto load_v = [&]() -> bool {
+                const int t = v_issued, vs = t % C::kVStages;
+                if (t >= C::kVStages &&
+                    !mbar_wait(bar(C::kBarVEmpty + vs), ((t / C::kVStages) - 1) & 1, ac))
+                    return false;
+                // V_t completes on P_t's barrier: the MMA issuer waits once for
+                // both.  The barrier's previous phase (tile t-2) must be over
+                // before it is armed for tile t: wait for PV_{t-2} (implied by
                 // the stage wait above when the V ring has at most 2 stages).
-                if (C::kVStages > 2 && j >= 2) {
-                    const int jp = j - 2;
-                    ok = mbar_wait(bar(C::kBarVEmpty + jp % C::kVStages),
-                                   (jp / C::kVStages) & 1, ac);
-                    if (!ok) break;
+                if (C::kVStages > 2 && t >= 2) {
+                    const int tp = t - 2;
+                    if (!mbar_wait(bar(C::kBarVEmpty + tp % C::kVStages), (tp / C::kVStages) & 1,
+                                   ac))
+                        return false;
                 }
-                const uint32_t pv_bar = bar(C::kBarPFull + (j & 1));
+                const uint32_t pv_bar = bar(C::kBarPFull + (t & 1));
                 mbar_arrive_expect_tx(pv_bar, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &tmV,
-                                pv_bar, c * 64, (kv_lo + j) * kBlockN, bh_kv);
-                v_issued = j + 1;
+                                pv_bar, c * 64, (vi.kv_lo + vj) * kBlockN, vi.bh_kv);
+                v_issued = t + 1;
+                advance(vr, vj, vi, v_done);
+                return true;
+            };
+            ok = load_k();
+            while (ok && !v_done) {
+                // K of the next tile first -- unless it opens a new item, whose Q
+                // may wait for an earlier item's output store: then V first.
+                const bool k_opens = !k_done && kj == 0;
+                if (!k_done && !k_opens) ok = load_k();
+                if (ok) ok = load_v();
+                if (ok && k_opens) ok = load_k();
             }
             if (!ok) {
                 // Let every copy already issued land before the CTA exits: the
-                // last arm of each stage is the only one not yet consumed.
-                drain_wait(bar(C::kBarQFull), 0);
-                for (int j = max(k_issued - C::kKStages, 0); j < k_issued; ++j)
-                    drain_wait(bar(C::kBarKFull + j % C::kKStages), (j / C::kKStages) & 1);
+                // last arm of each buffer is the only one not yet consumed.
+                for (int q = max(n_q - C::kQBufs, 0); q < n_q; ++q)
+                    drain_wait(bar(C::kBarQFull + q % C::kQBufs), (q / C::kQBufs) & 1);
+                for (int t = max(k_issued - C::kKStages, 0); t < k_issued; ++t)
+                    drain_wait(bar(C::kBarKFull + t % C::kKStages), (t / C::kKStages) & 1);
                 // (V loads complete on the P barriers, which may never fill
                 // after an abort: the drain then waits out its short limit.)
-                for (int j = max(v_issued - 2, 0); j < v_issued; ++j)
-                    drain_wait(bar(C::kBarPFull + (j & 1)), (j >> 1) & 1);
+                for (int t = max(v_issued - 2, 0); t < v_issued; ++t)
+                    drain_wait(bar(C::kBarPFull + (t & 1)), (t >> 1) & 1);
             }
         }
         __syncwarp();
@@ -335,10 +417,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
             constexpr uint32_t kIdPV = idesc_bf16_f32(kBlockM, D, false, true);
-            bool ok = mbar_wait(bar(C::kBarQFull), 0, ac);
-            tc_fence_after();
-
-            auto issue_pv = [&](int i, bool last) -> bool {
+            // PV of tile i (counted across items): `first` starts the item's O
+            // accumulator, `last` also signals the item's final O.  Every PV
+            // completes on ODone (the softmax waits there before a rescale).
+            auto issue_pv = [&](int i, bool first, bool last) -> bool {
                 const int pb = i & 1;
                 if (!mbar_wait(bar(C::kBarPFull + pb), (i >> 1) & 1, ac)) return false;
                 const int vs = i % C::kVStages;
@@ -349,32 +431,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
                     const uint64_t bdesc = sdesc_sw128(v_base + kk * 2048, C::kChunkBytes, 1024);
                     mma_ts(tmem + C::kColO, a_tmem + kk * 8, bdesc, kIdPV,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                           (!first || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(C::kBarVEmpty + vs));
-                mma_commit(bar(last ? C::kBarOFinal : C::kBarODone));
+                mma_commit(bar(C::kBarODone));
+                if (last) mma_commit(bar(C::kBarOFinal));
                 return true;
             };
 
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int ks = j % C::kKStages;
-                ok = mbar_wait(bar(C::kBarKFull + ks), (j / C::kKStages) & 1, ac);
-                if (!ok) break;
+            bool ok = true;
+            int n_q = 0, t = 0;   // items started, tiles whose S was issued
+            bool prev_first = false, prev_last = false;
+            for (int rnd = 0; ok; ++rnd) {
+                const int k = item_at(rnd);
+                if (k < 0) break;
+                const Item itm = decode(k);
+                const int qb = n_q % C::kQBufs;
+                if (!(ok = mbar_wait(bar(C::kBarQFull + qb), (n_q / C::kQBufs) & 1, ac))) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + (j & 1) * kBlockN;
-                const uint32_t k_base = sb + C::kOffK + ks * C::kTileBytes;
+                ++n_q;
+                const uint32_t q_base = sb + C::kOffQ + qb * C::kTileBytes;
+                for (int j = 0; j < itm.n_kv; ++j, ++t) {
+                    const int ks = t % C::kKStages;
+                    if (!(ok = mbar_wait(bar(C::kBarKFull + ks), (t / C::kKStages) & 1, ac))) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + (t & 1) * kBlockN;
+                    const uint32_t k_base = sb + C::kOffK + ks * C::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    const uint64_t adesc = sdesc_sw128(sb + C::kOffQ + off, 16, 1024);
-                    const uint64_t bdesc = sdesc_sw128(k_base + off, 16, 1024);
-                    mma_ss(d_tmem, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                        const uint64_t adesc = sdesc_sw128(q_base + off, 16, 1024);
+                        const uint64_t bdesc = sdesc_sw128(k_base + off, 16, 1024);
+                        mma_ss(d_tmem, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(C::kBarSFull + (t & 1)));
+                    mma_commit(bar(C::kBarKEmpty + ks));
+                    // The previous tile's PV (perhaps of the previous item).
+                    if (t >= 1 && !(ok = issue_pv(t - 1, prev_first, prev_last))) break;
+                    prev_first = j == 0;
+                    prev_last = j == itm.n_kv - 1;
                 }
-                mma_commit(bar(C::kBarSFull + (j & 1)));
-                mma_commit(bar(C::kBarKEmpty + ks));
-                if (j >= 1) ok = issue_pv(j - 1, false);
             }
-            if (ok) ok = issue_pv(n_kv - 1, true);
+            if (ok && t >= 1) ok = issue_pv(t - 1, prev_first, prev_last);
             if (!ok) {
                 mma_commit(bar(C::kBarDrain));
                 drain_wait(bar(C::kBarDrain), 0);
@@ -459,6 +557,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tma_store_wait_read();
         }
         __syncwarp();
+    } else if (fwd_persistent<EXT>() && warp == kWarpOStore) {
+        // ------------------------------------------------ output storer
+        // Stores each item's output tile (staged by the softmax warpgroups in
+        // the item's Q buffer) and hands the buffer back to the producer once
+        // the store has read it.
+        if (lane == 0) {
+            for (int rnd = 0;; ++rnd) {
+                const int k = item_at(rnd);
+                if (k < 0) break;
+                const Item itm = decode(k);
+                const int qb = rnd % C::kQBufs;
+                if (!mbar_wait(bar(C::kBarOStaged + qb), (rnd / C::kQBufs) & 1, ac)) break;
+                if (*abort_flag == 0) {
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_store_3d(&tmO, sb + C::kOffQ + qb * C::kTileBytes + c * C::kChunkBytes,
+                                     c * 64, itm.row_lo, itm.bh);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                }
+                mbar_arrive(bar(C::kBarQEmpty + qb));
+            }
+        }
+        __syncwarp();
     } else {
         // ---------------------------------------------- softmax warpgroups
         // Warpgroup wg handles keys [64 wg, 64 wg + 64) of every key tile for
@@ -469,17 +590,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // the next barrier and leave through it together).
         const int wg = warp >> 2;
         const int r = ((warp & 3) << 5) | lane;   // row within the tile == TMEM lane
-        const int q_row = qt * kBlockM + r;       // row within the head
-        const bool row_valid = q_row < p.N;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int col0 = wg * kHalfN;             // first key of this warpgroup
         float *red = reinterpret_cast<float *>(smem + C::kOffRed);   // [2][2][128]
+        bool ok = true;
+        int t = 0;   // key tiles over this block's items (the S / P buffer sequence)
+        for (int rnd = 0; ok; ++rnd) {
+        const int kitem = item_at(rnd);
+        if (kitem < 0) break;
+        const Item itm = decode(kitem);
+        const int qt = itm.qt, bh = itm.bh, kv_lo = itm.kv_lo, n_kv = itm.n_kv;
+        const int row_lo = itm.row_lo;
+        const int q_row = qt * kBlockM + r;       // row within the head
+        const bool row_valid = q_row < p.N;
         float m_run = -INFINITY;   // running max, log2 units
         float l_run = 0.f;         // this warpgroup's part of the row sum
-        bool ok = true;
 
-        for (int j = 0; j < n_kv; ++j) {
-            const int sbuf = j & 1;
+        for (int j = 0; j < n_kv; ++j, ++t) {
+            const int sbuf = t & 1;
             const uint32_t tS = tmem + lane_base + sbuf * kBlockN;
             const int key0 = (kv_lo + j) * kBlockN;
             const bool diag = CAUSAL && (kv_lo + j == qt);
@@ -495,7 +623,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             float xmul = kLog2e;
             float x[kHalfN];
             float mt_x = -INFINITY;
-            bool got = ok && mbar_wait_warp(bar(C::kBarSFull + sbuf), (j >> 1) & 1, ac);
+            bool got = ok && mbar_wait_warp(bar(C::kBarSFull + sbuf), (t >> 1) & 1, ac);
             if (got) {
                 tc_fence_after();
                 {
@@ -641,7 +769,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (__any_sync(0xffffffffu, need)) {
                 // O holds PV_0..PV_{j-1}; PV_{j-1} must have landed first.  Each
                 // warpgroup rescales its half of O's columns.
-                if (!mbar_wait_warp(bar(C::kBarODone), (j - 1) & 1, ac)) {
+                if (!mbar_wait_warp(bar(C::kBarODone), (t - 1) & 1, ac)) {
                     ok = false;   // leaves at the next barrier, with the other warpgroup
                 } else {
                     tc_fence_after();
@@ -657,31 +785,44 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
 
         // ------------------------------------------------------- epilogue
-        // Both warpgroups reach the barrier below exactly once, whatever
-        // happened in the loop.
-        if (ok) ok = mbar_wait_warp(bar(C::kBarOFinal), 0, ac);
-        float *lsum = red + (n_kv & 1) * 2 * kBlockM;   // buffer the last tile did not use
+        // Both warpgroups reach the barriers below exactly once per item,
+        // whatever happened in the loop.  O is staged (bf16, swizzled) in the
+        // item's Q buffer, which its S MMAs are done with.
+        if (ok) ok = mbar_wait_warp(bar(C::kBarOFinal), rnd & 1, ac);
+        float *lsum = red + (t & 1) * 2 * kBlockM;   // the buffer the item's last tile did not use
         if (ok) lsum[wg * kBlockM + r] = l_run;
         const bool fail = named_bar_or(2, kSoftThreads, !ok);
+        const uint32_t o_tile = sb + C::kOffQ + (rnd % C::kQBufs) * C::kTileBytes;
         if (!fail) {
             tc_fence_after();
             const float l_tot = l_run + lsum[(wg ^ 1) * kBlockM + r];
             const float inv_l = 1.f / l_tot;
             const uint32_t tO = tmem + lane_base + C::kColO;
-            if (wg == 0) o_stage<C::kOSplit, 0>(tO, inv_l, sb + C::kOffQ, r);
-            else o_stage<D - C::kOSplit, C::kOSplit>(tO + C::kOSplit, inv_l, sb + C::kOffQ, r);
+            if (wg == 0) o_stage<C::kOSplit, 0>(tO, inv_l, o_tile, r);
+            else o_stage<D - C::kOSplit, C::kOSplit>(tO + C::kOSplit, inv_l, o_tile, r);
             if (wg == 0 && p.lse && row_valid)
                 p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m_run + log2f(l_tot)) * kLn2;
             fence_proxy_async_smem();
         }
         tc_fence_before();
+        // (Also keeps the next item's first row-max writes off the row sums
+        // the other warpgroup reads above.)
         named_bar_sync(1, kSoftThreads);
-        if (threadIdx.x == 0 && !fail && *abort_flag == 0) {
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_store_3d(&tmO, sb + C::kOffQ + c * C::kChunkBytes, c * 64, qt * kBlockM, bh);
-            tma_store_commit();
-            tma_store_wait_read();
+        if (fail) {
+            ok = false;
+            break;
         }
+        if constexpr (fwd_persistent<EXT>()) {
+            mbar_arrive(bar(C::kBarOStaged + rnd % C::kQBufs));   // the storer warp takes it from here
+        } else {
+            if (threadIdx.x == 0 && *abort_flag == 0) {
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_store_3d(&tmO, o_tile + c * C::kChunkBytes, c * 64, row_lo, bh);
+                tma_store_commit();
+                tma_store_wait_read();
+            }
+        }
+        }   // items
     }
 
     tc_fence_before();
@@ -748,7 +889,7 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     prm.scale = pb.scale;
     prm.scale_log2 = pb.scale * kLog2e;
     prm.window = pb.causal ? pb.window : 0;
-    const unsigned grid = static_cast<unsigned>(prm.n_qtiles * BH);
+    const long long n_items = static_cast<long long>(prm.n_qtiles) * BH;
     int ext = 0;
     if (pb.bias || pb.emit) {
         // The staged variant maps the [N, N] planes as tensors of 128 x 32
@@ -763,6 +904,17 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
             ext = 1;
     }
     if (ext != 2) m.bias = m.emit = m.q;   // unused by the kernel
+    // The plain forward runs one persistent block per SM (each holds most of
+    // an SM's shared memory and all of its TMEM); the residual variants one
+    // block per (query tile, head).
+    unsigned grid = static_cast<unsigned>(n_items);
+    if (ext == 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        if (sms > 0 && n_items > sms) grid = static_cast<unsigned>(sms);
+    }
     switch (pb.D) {
     case 64: return launch_d<64>(pb.causal, ext, m, prm, grid, stream);
     case 80: return launch_d<80>(pb.causal, ext, m, prm, grid, stream);
