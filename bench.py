@@ -360,143 +360,152 @@ def run_ours(args):
     sh = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # phases: list of (label, fn, flops, algorithmic bytes) run in order per step
-    phases = []
-    host_inputs, dev_inputs, results = [], [], []
-    if kind == "decode":
-        from tiled_attention_02_gb300.inputs import make_decode
-        x = make_decode(B, Hq, Hkv, N, D, seed=rank)
-        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-        o = torch.empty_like(q)
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-        ws = torch.empty(max(ta.attn_decode_workspace_size(B, Hq, Hkv, N, D), 256),
-                         dtype=torch.uint8, device=dev)
-
-        def dec():
-            s = ta.raw_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                   lse.data_ptr(), B, Hq, Hkv, N, D, scale, ws.data_ptr(),
-                                   ws.numel(), sh)
-            assert s == 0, s
-        # algorithmic bytes: the K/V cache once, the query rows, O and LSE
-        dec_bytes = 2 * (B * Hkv * N * D) * 2 + 2 * (B * Hq * D) * 2 + B * Hq * 4
-        phases.append(("decode", dec, 4.0 * B * Hq * N * D, dec_bytes))
-        host_inputs += [x["q"], x["k"], x["v"]]
-        dev_inputs += [q, k, v]
-        results = [o]
-    elif kind == "chain_train":
-        # 4-layer block, forward then backward: every layer keeps its emitted
-        # logits (the next layer's bias, needed again by the backward), and
-        # one fp32 buffer carries the logit gradient down the block in place.
-        L = W["layers"]
-        layers = make_chain(B, Hq, Hkv, N, D, layers=L, seed=rank, with_do=True)
-        dl = [{n: x[n].to(dev) for n in ("q", "k", "v", "do")} for x in layers]
-        outs = [(torch.empty_like(x["q"]),
-                 torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
-        S = [torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev) for _ in range(L - 1)]
-        gbuf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
-        grads = [(torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
-                 for x in dl]
-        ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
-                         dtype=torch.uint8, device=dev)
-        kept = B * Hq * (N * (N + 1) // 2 if causal else N * N) * 4
-        for i in range(L):
-            def layer_f(i=i):
-                x, (o, lse) = dl[i], outs[i]
-                st = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
-                                     S[i - 1].data_ptr() if i > 0 else None, o.data_ptr(),
-                                     lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
-                                     S[i].data_ptr() if i < L - 1 else None, sh)
-                assert st == 0, st
-            phases.append((f"fwd{i}", layer_f, attn_flops(B, Hq, N, D, causal),
-                           chain_layer_bytes(W, i)))
-        io_b = 5 * (B * Hq * N * D) * 2 + 2 * 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-        for i in reversed(range(L)):
-            def layer_b(i=i):
-                x, (o, lse) = dl[i], outs[i]
-                dq, dk, dv = grads[i]
-                st = ta.raw_attn_bwd_residual(
-                    x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
-                    lse.data_ptr(), x["do"].data_ptr(), S[i - 1].data_ptr() if i > 0 else None,
-                    gbuf.data_ptr() if i < L - 1 else None, dq.data_ptr(), dk.data_ptr(),
-                    dv.data_ptr(), gbuf.data_ptr() if i > 0 else None, B, Hq, Hkv, N, D, scale,
-                    causal, ws.data_ptr(), ws.numel(), sh)
-                assert st == 0, st
-            by = io_b + kept * ((i > 0) + (i < L - 1) + (i > 0))
-            phases.append((f"bwd{i}", layer_b, bwd_flops(B, Hq, N, D, causal), by))
-        for i, x in enumerate(layers):
-            for n in ("q", "k", "v", "do"):
-                host_inputs.append(x[n])
-                dev_inputs.append(dl[i][n])
-        results = [grads[0][0]]
-    elif kind == "chain":
-        layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
-        dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
-        outs = [(torch.empty_like(x["q"]),
-                 torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
-        buf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
-        L = W["layers"]
-        for i in range(L):
-            def layer(i=i):
-                x, (o, lse) = dl[i], outs[i]
-                s = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
-                                    buf.data_ptr() if i > 0 else None, o.data_ptr(),
-                                    lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
-                                    buf.data_ptr() if i < L - 1 else None, sh)
-                assert s == 0, s
-            phases.append((f"layer{i}", layer, attn_flops(B, Hq, N, D, causal),
-                           chain_layer_bytes(W, i)))
-        for i, x in enumerate(layers):
-            for n in ("q", "k", "v"):
-                host_inputs.append(x[n])
-                dev_inputs.append(dl[i][n])
-        results = [outs[-1][0]]
-    else:
-        x = make_qkv(B, Hq, Hkv, N, D, seed=rank, with_do=(kind == "fwd_bwd"))
-        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-        o = torch.empty_like(q)
-        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-
-        window = W.get("window")
-
-        def fwd():
-            if window:
-                s = ta.raw_attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
-                                           o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
-                                           window, None, sh)
-            else:
-                s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
-                                    o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
-                                    causal, None, sh)
-            assert s == 0, s
-        io_bytes = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-        phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal, window), io_bytes))
-        host_inputs += [x["q"], x["k"], x["v"]]
-        dev_inputs += [q, k, v]
-        results = [o]
-        if kind == "fwd_bwd":
-            do = x["do"].to(dev)
-            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-            ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+    def build_workload():
+        """One independent set of device buffers and the phases that run on
+        them: (phases, host inputs, device inputs, results)."""
+        # phases: list of (label, fn, flops, algorithmic bytes) run in order per step
+        phases = []
+        host_inputs, dev_inputs, results = [], [], []
+        if kind == "decode":
+            from tiled_attention_02_gb300.inputs import make_decode
+            x = make_decode(B, Hq, Hkv, N, D, seed=rank)
+            q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+            o = torch.empty_like(q)
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(ta.attn_decode_workspace_size(B, Hq, Hkv, N, D), 256),
                              dtype=torch.uint8, device=dev)
 
-            def bwd():
-                if window:
-                    s = ta.raw_attn_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                               o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B,
-                                               Hq, Hkv, N, D, scale, window, ws.data_ptr(),
-                                               ws.numel(), sh)
-                else:
-                    s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                        lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
-                                        dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, D, scale,
-                                        causal, ws.data_ptr(), ws.numel(), sh)
+            def dec():
+                s = ta.raw_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), B, Hq, Hkv, N, D, scale, ws.data_ptr(),
+                                       ws.numel(), sh)
                 assert s == 0, s
-            bwd_bytes = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-            phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal, window), bwd_bytes))
-            host_inputs.append(x["do"])
-            dev_inputs.append(do)
-            results = [dq, dk, dv]
+            # algorithmic bytes: the K/V cache once, the query rows, O and LSE
+            dec_bytes = 2 * (B * Hkv * N * D) * 2 + 2 * (B * Hq * D) * 2 + B * Hq * 4
+            phases.append(("decode", dec, 4.0 * B * Hq * N * D, dec_bytes))
+            # The K/V cache is state that stays on the device across decode
+            # steps; a step's input is its query rows.
+            host_inputs += [x["q"]]
+            dev_inputs += [q]
+            results = [o]
+        elif kind == "chain_train":
+            # 4-layer block, forward then backward: every layer keeps its emitted
+            # logits (the next layer's bias, needed again by the backward), and
+            # one fp32 buffer carries the logit gradient down the block in place.
+            L = W["layers"]
+            layers = make_chain(B, Hq, Hkv, N, D, layers=L, seed=rank, with_do=True)
+            dl = [{n: x[n].to(dev) for n in ("q", "k", "v", "do")} for x in layers]
+            outs = [(torch.empty_like(x["q"]),
+                     torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
+            S = [torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev) for _ in range(L - 1)]
+            gbuf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
+            grads = [(torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
+                     for x in dl]
+            ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+                             dtype=torch.uint8, device=dev)
+            kept = B * Hq * (N * (N + 1) // 2 if causal else N * N) * 4
+            for i in range(L):
+                def layer_f(i=i):
+                    x, (o, lse) = dl[i], outs[i]
+                    st = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                         S[i - 1].data_ptr() if i > 0 else None, o.data_ptr(),
+                                         lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                         S[i].data_ptr() if i < L - 1 else None, sh)
+                    assert st == 0, st
+                phases.append((f"fwd{i}", layer_f, attn_flops(B, Hq, N, D, causal),
+                               chain_layer_bytes(W, i)))
+            io_b = 5 * (B * Hq * N * D) * 2 + 2 * 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+            for i in reversed(range(L)):
+                def layer_b(i=i):
+                    x, (o, lse) = dl[i], outs[i]
+                    dq, dk, dv = grads[i]
+                    st = ta.raw_attn_bwd_residual(
+                        x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), x["do"].data_ptr(), S[i - 1].data_ptr() if i > 0 else None,
+                        gbuf.data_ptr() if i < L - 1 else None, dq.data_ptr(), dk.data_ptr(),
+                        dv.data_ptr(), gbuf.data_ptr() if i > 0 else None, B, Hq, Hkv, N, D, scale,
+                        causal, ws.data_ptr(), ws.numel(), sh)
+                    assert st == 0, st
+                by = io_b + kept * ((i > 0) + (i < L - 1) + (i > 0))
+                phases.append((f"bwd{i}", layer_b, bwd_flops(B, Hq, N, D, causal), by))
+            for i, x in enumerate(layers):
+                for n in ("q", "k", "v", "do"):
+                    host_inputs.append(x[n])
+                    dev_inputs.append(dl[i][n])
+            results = [grads[0][0]]
+        elif kind == "chain":
+            layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
+            dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
+            outs = [(torch.empty_like(x["q"]),
+                     torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
+            buf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
+            L = W["layers"]
+            for i in range(L):
+                def layer(i=i):
+                    x, (o, lse) = dl[i], outs[i]
+                    s = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                        buf.data_ptr() if i > 0 else None, o.data_ptr(),
+                                        lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                        buf.data_ptr() if i < L - 1 else None, sh)
+                    assert s == 0, s
+                phases.append((f"layer{i}", layer, attn_flops(B, Hq, N, D, causal),
+                               chain_layer_bytes(W, i)))
+            for i, x in enumerate(layers):
+                for n in ("q", "k", "v"):
+                    host_inputs.append(x[n])
+                    dev_inputs.append(dl[i][n])
+            results = [outs[-1][0]]
+        else:
+            x = make_qkv(B, Hq, Hkv, N, D, seed=rank, with_do=(kind == "fwd_bwd"))
+            q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+            o = torch.empty_like(q)
+            lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+
+            window = W.get("window")
+
+            def fwd():
+                if window:
+                    s = ta.raw_attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
+                                               o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                               window, None, sh)
+                else:
+                    s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
+                                        o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                        causal, None, sh)
+                assert s == 0, s
+            io_bytes = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+            phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal, window), io_bytes))
+            host_inputs += [x["q"], x["k"], x["v"]]
+            dev_inputs += [q, k, v]
+            results = [o]
+            if kind == "fwd_bwd":
+                do = x["do"].to(dev)
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+                                 dtype=torch.uint8, device=dev)
+
+                def bwd():
+                    if window:
+                        s = ta.raw_attn_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                   o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B,
+                                                   Hq, Hkv, N, D, scale, window, ws.data_ptr(),
+                                                   ws.numel(), sh)
+                    else:
+                        s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                            dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                            causal, ws.data_ptr(), ws.numel(), sh)
+                    assert s == 0, s
+                bwd_bytes = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+                phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal, window), bwd_bytes))
+                host_inputs.append(x["do"])
+                dev_inputs.append(do)
+                results = [dq, dk, dv]
+        return phases, host_inputs, dev_inputs, results
+
+    phases, host_inputs, dev_inputs, results = build_workload()
+
     launches = {"fwd": 1, "bwd": 3, "decode": 2}
     launches.update({f"bwd{i}": 3 for i in range(8)})
     launches_per_step = sum(launches.get(lbl, 1) for lbl, *_ in phases)
@@ -544,34 +553,90 @@ def run_ours(args):
     value = world * flops_step / (ms_step * 1e-3) / 1e12
 
     # ------------------------------------------------------------ e2e
+    # Every step copies its inputs from pinned host memory to the device and
+    # its results back, all inside the timed region.  Steps are pipelined the
+    # way a host program would run them: two sets of device buffers, the
+    # upload of step i+1 and the download of step i-1 on two copy streams
+    # while step i computes.  The serial form (copy in, compute, copy out, on
+    # one stream) is timed too and reported beside it.
     e2e = None
     if not args.no_e2e:
         pinned = [t.pin_memory() for t in host_inputs]
         outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
         h2d = sum(t.numel() * t.element_size() for t in pinned)
         d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        phases_b, _, dev_inputs_b, results_b = build_workload()
+        sets = [(phases, dev_inputs, results), (phases_b, dev_inputs_b, results_b)]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        n_e2e = max(4, min(args.steps, 20))
 
-        def e2e_step():
+        def serial_step():
             for d, h in zip(dev_inputs, pinned):
                 d.copy_(h, non_blocking=True)
             step()
             for h, d in zip(outs_h, results):
                 h.copy_(d, non_blocking=True)
 
+        def pipelined(n):
+            computed = [None, None]   # event: the set's last compute is done
+            downloaded = [None, None]  # event: the set's results have been copied out
+            start = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            up.wait_event(start)
+            last = None
+            for i in range(n):
+                ph, di, re = sets[i % 2]
+                with torch.cuda.stream(up):
+                    if computed[i % 2] is not None:
+                        up.wait_event(computed[i % 2])   # step i-2 has read these inputs
+                    for d, h in zip(di, pinned):
+                        d.copy_(h, non_blocking=True)
+                    loaded = torch.cuda.Event()
+                    loaded.record(up)
+                stream.wait_event(loaded)
+                if downloaded[i % 2] is not None:
+                    stream.wait_event(downloaded[i % 2])   # step i-2's results are out
+                for _, fn, _, _ in ph:
+                    fn()
+                done = torch.cuda.Event()
+                done.record(stream)
+                computed[i % 2] = done
+                with torch.cuda.stream(down):
+                    down.wait_event(done)
+                    for h, d in zip(outs_h, re):
+                        h.copy_(d, non_blocking=True)
+                    last = torch.cuda.Event()
+                    last.record(down)
+                downloaded[i % 2] = last
+            stream.wait_event(last)
+            end = torch.cuda.Event(enable_timing=True)
+            end.record(stream)
+            return start, end
+
         for _ in range(2):
-            e2e_step()
+            serial_step()
+        pipelined(2)
         torch.cuda.synchronize(dev)
-        n_e2e = max(3, min(args.steps, 20))
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n_e2e):
-            e2e_step()
+            serial_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        serial_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
+        barrier(world)
+        p0, p1 = pipelined(n_e2e)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(p0.elapsed_time(p1) / n_e2e, world, dev)
+        assert ta.attn_last_device_status() == 0
         e2e = {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": n_e2e,
+               "overlap": "two device buffer sets; step i+1's upload and step i-1's download "
+                          "run on two copy streams while step i computes",
+               "serial_ms_per_step": serial_ms,
+               "serial_value": world * flops_step / (serial_ms * 1e-3) / 1e12}
 
     # ------------------------------------------------------- roofline
     # The dominant kernel by device time decides the roofline entry; every
