@@ -139,3 +139,38 @@ def test_parity_full_size_sampled(ta, orc, name, B, Hq, Hkv, N, D, causal):
     # properties at every row: finite, and LSE within its bounds
     # (max logit <= LSE <= max logit + ln |J_i|, so LSE <= |s|_max + ln N)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+# More (query tile, head) items than SMs, so that the plain forward's
+# persistent blocks each walk several items (the rings, S/P buffers and output
+# buffers continue across item boundaries), with a ragged last tile, grouped
+# heads, odd head dims and a sliding window.  Outputs start as NaN: every item
+# of every block must be written.
+MULTI_ITEM = [
+    # B, Hq, Hkv, N, D, causal, window
+    (3, 24, 8, 1000, 128, True, None),
+    (3, 24, 8, 1000, 80, False, None),
+    (2, 40, 40, 700, 64, True, None),
+    (2, 48, 16, 1500, 96, True, 300),
+]
+
+
+@pytest.mark.parametrize("case", MULTI_ITEM,
+                         ids=[f"B{c[0]}H{c[1]}kv{c[2]}N{c[3]}D{c[4]}{'c' if c[5] else 'nc'}"
+                              f"{'W' + str(c[6]) if c[6] else ''}" for c in MULTI_ITEM])
+def test_parity_more_items_than_sms(ta, orc, case):
+    B, Hq, Hkv, N, D, causal, window = case
+    n_items = B * Hq * ((N + 127) // 128)
+    assert n_items > torch.cuda.get_device_properties(0).multi_processor_count
+    x = make_qkv(B, Hq, Hkv, N, D, seed=B * N + D)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, N), float("nan"), device="cuda")
+    ta.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, window=window)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    ref = orc.forward(to_oracle(x["q"]), to_oracle(x["k"]), to_oracle(x["v"]),
+                      scale=1 / math.sqrt(D), causal=causal, window=window)
+    check_o(o, ref["o"], f"{case}")
+    check_lse(lse, ref["lse"], f"{case}")
