@@ -38,7 +38,8 @@ if ROOT not in sys.path:
 METRIC = "attention TFLOPS (4·B·H·N²·D, causal/2) and % of GB300 dense BF16 peak"
 WORKLOAD = dict(name="causal_fwd_bwd_B1_H16_N16384_D128", B=1, Hq=16, Hkv=16, N=16384, D=128,
                 causal=True)
-L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2
+L2_BYTES = 129 << 20         # GB300 L2
+L2_FLUSH_BYTES = 256 << 20   # > L2
 
 
 def attn_flops(B, H, N, D, causal, window=None):
@@ -282,8 +283,7 @@ def config_block(world, W=None):
     W = W or WORKLOAD
     cfg = {"workload": W["name"], "B": W["B"], "H": W["Hq"], "Hkv": W["Hkv"], "N": W["N"],
            "D": W["D"], "causal": W["causal"], "scale": 1 / math.sqrt(W["D"]),
-           "parallelism": f"replicas x{world} (independent problems, no collective)",
-           "l2": "flushed between timed steps (256 MB write)"}
+           "parallelism": f"replicas x{world} (independent problems, no collective)"}
     if W.get("kind") in ("chain", "chain_train"):
         cfg["layers"] = W["layers"]
     if W.get("window"):
@@ -532,8 +532,14 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)   # let the sampler start before the load
+    # Between timed steps either flush L2 (write a buffer larger than it) or
+    # rely on a step's own traffic being larger than L2 (more than twice its
+    # size), which leaves nothing of the previous step resident.
+    bytes_per_step = sum(ph[3] for ph in phases)
+    do_flush = args.l2 == "flush" or (args.l2 == "auto" and bytes_per_step <= 2 * L2_BYTES)
     for i in range(args.steps):
-        flush.fill_(float(i))       # untimed: evicts the previous step's data from L2
+        if do_flush:
+            flush.fill_(float(i))   # untimed: evicts the previous step's data from L2
         ev[i][0].record(stream)
         for j, (_, fn, _, _) in enumerate(phases):
             fn()
@@ -718,7 +724,12 @@ def run_ours(args):
                                  "decode": "one decode step (stream-K over one block per SM, then merge)",
                                  "chain_train": "four chained layers forward, then backward "
                                                 "through the block (fp32 residual and gradient)",
-                                 "chain": "four chained forward layers, fp32 residual in place"}[kind]),
+                                 "chain": "four chained forward layers, fp32 residual in place"}[kind],
+                           l2=(f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)"
+                               if do_flush else
+                               f"no flush: inputs larger than L2 (a step moves "
+                               f"{bytes_per_step / 2**20:.0f} MB, over twice the "
+                               f"{L2_BYTES >> 20} MB L2)")),
             "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
             "hbm_gbs_step": world * bytes_step / (ms_step * 1e-3) / 1e9,
             "roofline": roof, "kernels": kernels, "clocks": clocks,
@@ -742,6 +753,9 @@ def main():
     ap.add_argument("--workload", default="step", choices=["step", *EXTRA_WORKLOADS],
                     help="step (default): the causal fwd+bwd line; others for manual runs")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
+                    help="between timed steps: flush L2, or not (auto: flush unless a step's "
+                         "algorithmic bytes exceed twice the L2 size)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-min-s", type=float, default=10.0)
     ap.add_argument("--cpu-max-s", type=float, default=30.0)
