@@ -174,3 +174,23 @@ def test_parity_more_items_than_sms(ta, orc, case):
                       scale=1 / math.sqrt(D), causal=causal, window=window)
     check_o(o, ref["o"], f"{case}")
     check_lse(lse, ref["lse"], f"{case}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_parity_growing_row_max(ta, orc, D, causal):
+    """Keys ramped by position: a row's logits grow by about 8 (natural units,
+    11.5 in log2) per 128-key tile, so each new tile raises the row max past
+    the lazy-rescale threshold and the running output is rescaled at every
+    tile, on top of the score MMAs running ahead of the PV MMAs."""
+    B, H, N = 2, 3, 1000
+    x = make_qkv(B, H, H, N, D, seed=11)
+    c = 8.0 / math.sqrt(D)   # scale * D * c / 128 = 8 / 128 per key
+    ramp = (torch.arange(N, dtype=torch.float32) / 128.0).view(1, 1, N, 1)
+    x["q"] = (1.0 + 0.25 * x["q"].float()).to(torch.bfloat16)
+    x["k"] = (c * ramp + 0.25 * x["k"].float()).to(torch.bfloat16)
+    o, lse = run_fwd(ta, x, causal=causal)
+    ref = oracle_fwd(orc, x, causal, 1 / math.sqrt(D))
+    assert float(ref["lse"].max()) > 40.0   # the growth is really there
+    check_o(o, ref["o"], f"growing max D{D} causal={causal}")
+    check_lse(lse, ref["lse"], f"growing max D{D} causal={causal}")
