@@ -207,6 +207,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmQ,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The merge kernel's blocks may be scheduled beside this grid's from now
+    // on; they wait (griddep_wait) until this grid has finished.
+    if (t == 0) griddep_launch_dependents();
 
     if (warp == kWarpProducer) {
         // ------------------------------------------------------ TMA producer
@@ -487,6 +490,9 @@ decode_merge_kernel(const float *__restrict__ m_part, const float *__restrict__ 
                     const float *__restrict__ o_part, __nv_bfloat16 *__restrict__ o,
                     float *__restrict__ lse, int rows, int G, int D, int spg, long long T,
                     int grid) {
+    // Launched as a programmatic dependent of the split kernel: its partials
+    // are complete and visible once this returns.
+    griddep_wait();
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -544,9 +550,25 @@ cudaError_t launch_d(const DecProblem &pb, int *status, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int rows = pb.B * pb.Hq;
-    decode_merge_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(
-        pb.m_part, pb.l_part, pb.o_part, static_cast<__nv_bfloat16 *>(pb.o), pb.lse, rows, prm.G,
-        D, prm.spg, prm.T, pb.grid);
+    // Programmatic stream serialization: the merge's blocks start while the
+    // split kernel runs and wait in the kernel for it to finish, which hides
+    // the second launch's latency.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, static_cast<const float *>(pb.m_part),
+                           static_cast<const float *>(pb.l_part),
+                           static_cast<const float *>(pb.o_part),
+                           static_cast<__nv_bfloat16 *>(pb.o), pb.lse, rows, prm.G, static_cast<int>(D),
+                           prm.spg, prm.T, static_cast<int>(pb.grid));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
