@@ -32,6 +32,18 @@
 namespace tattn {
 namespace {
 
+// Programmatic dependent launch.  griddep_launch_dependents lets a kernel
+// launched after this one with programmatic stream serialization start its
+// blocks now (once every block of this grid has signalled or exited);
+// griddep_wait blocks until the grids this one depends on have completed and
+// their memory operations are visible (a no-op without the dependency).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 constexpr int kKeys = 128;           // keys per stage: the MMA M of S^T
 constexpr int kHeads = 16;           // query heads of a group, padded: the MMA N
 constexpr int kThreads = 192;        // warps 0-3 softmax / output, 4 producer, 5 MMA

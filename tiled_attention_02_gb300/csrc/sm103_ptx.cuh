@@ -37,21 +37,6 @@ __device__ __forceinline__ uint32_t lane_id() {
     return l;
 }
 
-// ------------------------------------------- programmatic dependent launch
-
-// Lets a kernel launched after this one with programmatic stream
-// serialization start its blocks now (once every block of this grid has
-// signalled or exited); they wait in griddep_wait for this grid to finish.
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Waits until the grids this one depends on have completed and their memory
-// operations are visible (a no-op when launched without the dependency).
-__device__ __forceinline__ void griddep_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
