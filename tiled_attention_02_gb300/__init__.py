@@ -9,10 +9,19 @@ fallback: if the library is missing the calls raise.
 
 Functions mirror the C entry points:
 
-* :func:`attn_fwd` -- ``attn_fwd`` (O, LSE, optional bias in / logits out)
-* :func:`attn_bwd` -- ``attn_bwd`` (dQ, dK, dV by recomputation)
-* :func:`attn_bwd_workspace_size`, :func:`attn_last_device_status`,
-  :func:`attn_status_string`
+* :func:`attn_fwd` -- ``attn_fwd`` / ``attn_fwd_window`` (O, LSE, optional
+  fp32 bias in / logits out, optional causal sliding window)
+* :func:`attn_bwd` -- ``attn_bwd`` / ``attn_bwd_window`` / ``attn_bwd_residual``
+  (dQ, dK, dV by recomputation; with a bias, the logit gradient in and out)
+* :func:`attn_bwd_noalloc` -- ``attn_bwd_noalloc`` (the backward with the
+  library's fixed scratch instead of a caller workspace)
+* :func:`attn_decode` -- ``attn_decode`` (one new query row per head against
+  an N-row K/V cache)
+* :func:`attn_bwd_workspace_size`, :func:`attn_decode_workspace_size`,
+  :func:`attn_last_device_status`, :func:`attn_status_string`
+
+The ``raw_*`` functions take plain integers (device pointers, sizes, stream
+handle) and return the status code, for tests of the C boundary itself.
 """
 from __future__ import annotations
 
