@@ -50,6 +50,8 @@
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
+#include <algorithm>
+
 namespace tattn {
 namespace {
 
@@ -149,6 +151,7 @@ struct FwdParams {
     float scale;        // scale of QK^T
     float scale_log2;   // scale * log2(e)
     int window;         // causal sliding window W (key j kept iff i - W < j), 0 = none
+    int hchunk;         // causal item order: heads per chunk (BH: a single chunk)
 };
 
 // O *= alpha on NC consecutive TMEM columns of this thread's row.
@@ -235,12 +238,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     auto decode = [&](int k) -> Item {
         Item it;
         // Causal: heaviest tiles first (item 0 is the last query tile of
-        // head 0), heads fastest.  Otherwise every item weighs the same, and
-        // query tiles go fastest so that the blocks running at once share a
-        // few heads' K/V in L2 instead of each streaming its own from HBM.
+        // head 0), heads fastest, within chunks of hchunk heads taken one
+        // after another (one chunk unless all heads' K/V is well over L2, so
+        // that the items running at once share a few heads' K/V).  Otherwise
+        // every item weighs the same, and query tiles go fastest so that the
+        // blocks running at once share a few heads' K/V in L2 instead of each
+        // streaming its own from HBM.
         if (CAUSAL) {
-            it.qt = p.n_qtiles - 1 - k / p.BH;
-            it.bh = k % p.BH;
+            if (p.hchunk >= p.BH) {
+                it.qt = p.n_qtiles - 1 - k / p.BH;
+                it.bh = k % p.BH;
+            } else {
+                const int per_chunk = p.hchunk * p.n_qtiles;
+                const int c = k / per_chunk;
+                const int nh = min(p.hchunk, p.BH - c * p.hchunk);   // heads of this chunk
+                const int kk = k - c * per_chunk;
+                it.qt = p.n_qtiles - 1 - kk / nh;
+                it.bh = c * p.hchunk + kk % nh;
+            }
         } else {
             it.qt = k % p.n_qtiles;
             it.bh = k / p.n_qtiles;
@@ -890,6 +905,23 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     prm.scale_log2 = pb.scale * kLog2e;
     prm.window = pb.causal ? pb.window : 0;
     const long long n_items = static_cast<long long>(prm.n_qtiles) * BH;
+    // Causal item order: one chunk of all heads unless their K/V is over
+    // twice the L2; then chunks whose K/V is about half the L2, so that the
+    // items running at once share a few heads' K/V (measured, D128 causal:
+    // B8 H32 N8192 4.78 -> 3.78 ms, where the 152 items running at once
+    // were otherwise 152 different heads; B4 H16 N16384 and B1 H16 N65536
+    // the same or slightly faster).
+    prm.hchunk = static_cast<int>(BH);
+    {
+        int dev = 0, l2 = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
+            l2 = 128 << 20;
+        const double head_kv = static_cast<double>(pb.N) * pb.D * 4.0 / (pb.Hq / pb.Hkv);   // per query head
+        if (pb.causal && head_kv * static_cast<double>(BH) > 2.0 * l2)
+            prm.hchunk = static_cast<int>(
+                std::max<long long>(1, std::min<long long>(BH, static_cast<long long>(0.5 * l2 / head_kv))));
+    }
     int ext = 0;
     if (pb.bias || pb.emit) {
         // The staged variant maps the [N, N] planes as tensors of 128 x 32
