@@ -17,6 +17,7 @@ __device__ int g_status_word;
 
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices] = {};
+DeviceInfo g_dev_info[kMaxDevices] = {};   // sms == 0: not yet queried
 std::mutex g_mu;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -102,6 +103,25 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int Hkv, int N, int D) {
     w.dv_acc = w.dk_acc + round256(kvrows * D * sizeof(float));
     w.total = w.dv_acc + round256(kvrows * D * sizeof(float));
     return w;
+}
+
+bool device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev_info[dev];
+    if (d.sms == 0) {
+        int sms = 0, l2 = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0)
+            return false;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
+            l2 = 128 << 20;
+        d.l2_bytes = l2;
+        d.sms = sms;
+    }
+    *out = d;
+    return true;
 }
 
 int *device_status_ptr() {
@@ -268,10 +288,9 @@ attn_status attn_decode(const void *q, const void *k, const void *v, void *o, fl
         return ATTN_ERR_INVALID;
     const DecWorkspace wl = decode_workspace_layout(B, Hq, Hkv, D);
     if (workspace_bytes < wl.total) return ATTN_ERR_INVALID;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return ATTN_ERR_CUDA;
+    DeviceInfo di;
+    if (!device_info(&di)) return ATTN_ERR_CUDA;
+    const int sms = di.sms;
     // One persistent block per SM (each holds most of an SM's shared
     // memory), never more blocks than 128-key stages.
     const long long stages = decode_stages(B, Hkv, N);

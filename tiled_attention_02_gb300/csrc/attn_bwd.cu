@@ -260,13 +260,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // heaviest key tiles first within a chunk (under the causal mask tile 0
     // sees every query tile), so that the blocks running at once share a few
     // heads' Q, dO and dQ accumulator in L2.
-    const int per_head = p.n_tiles * p.hsplit;               // blocks of one kv head
-    const int chunk = blockIdx.x / (p.hchunk * per_head);
-    const int nh = min(p.hchunk, p.BHkv - chunk * p.hchunk);  // kv heads of this chunk
-    const int rem = blockIdx.x - chunk * p.hchunk * per_head;
-    const int kt = rem / (nh * p.hsplit);
-    const int bh_kv = chunk * p.hchunk + (rem % (nh * p.hsplit)) / p.hsplit;
-    const int hs = rem % p.hsplit;                 // which share of the group's query heads
+    // blockIdx.y is the chunk of hchunk kv heads (chunks run one after
+    // another: blocks are dispatched in order of their linear index).
+    const int kt = blockIdx.x / (p.hchunk * p.hsplit);
+    const int bh_kv = blockIdx.y * p.hchunk + (blockIdx.x % (p.hchunk * p.hsplit)) / p.hsplit;
+    const int hs = blockIdx.x % p.hsplit;          // which share of the group's query heads
     const int hper = p.group / p.hsplit;           // query heads of this block
     const int b = bh_kv / p.Hkv, g = bh_kv % p.Hkv;
     // Query tiles q_lo .. q_lo + nq - 1 see this key tile: from the diagonal
@@ -974,7 +972,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 template <int D, bool RES>
-cudaError_t launch_main(const CUtensorMap (&m)[10], const BwdParams &prm, unsigned grid,
+cudaError_t launch_main(const CUtensorMap (&m)[10], const BwdParams &prm, dim3 grid,
                         bool causal, cudaStream_t stream) {
     using C = BwdCfg<D, RES>;
     auto kern = causal ? bwd_main_kernel<D, true, RES> : bwd_main_kernel<D, false, RES>;
@@ -992,15 +990,11 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     const long long BHkv = static_cast<long long>(pb.B) * pb.Hkv;
     const int n_tiles = pb.NP / kTile;
 
-    // 1. Delta, LSE*log2(e), zeroed dQ accumulator.
-    bwd_pre_kernel<D><<<dim3(static_cast<unsigned>(BH), n_tiles), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(pb.o), static_cast<const __nv_bfloat16 *>(pb.dO),
-        pb.lse, pb.lse2, pb.delta, pb.dq_acc, pb.N, pb.NP);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // The host work (device queries, tensor maps) comes first and the three
+    // launches back to back, so that the GPU does not wait between them.
+    cudaError_t e = cudaSuccess;
 
-    // 2. main kernel.
-    // maps: q, k, v, dO, dK, dV, dQ accumulator, bias, incoming and outgoing
+    // Main kernel maps: q, k, v, dO, dK, dV, dQ accumulator, bias, incoming and outgoing
     // logit gradients (the last three: [B*Hq, N query rows, N keys] fp32 in
     // 32 x 32 boxes; a map of the first given one stands in for absent ones).
     CUtensorMap m[10];
@@ -1015,10 +1009,9 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     const bool res = pb.bias || pb.grad_in || pb.grad_out;
     // Split a key tile's query heads over blocks when the grid would
     // otherwise leave SMs idle or run a few long blocks (grouped heads only).
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return cudaErrorInvalidValue;
+    DeviceInfo di;
+    if (!device_info(&di)) return cudaErrorInvalidValue;
+    const int sms = di.sms;
     const int group = pb.Hq / pb.Hkv;
     const int hsplit =
         (group > 1 && pb.dk_acc && static_cast<long long>(n_tiles) * BHkv < 2LL * sms) ? group : 1;
@@ -1069,16 +1062,27 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     // running at once keep theirs resident (measured, D128 causal: B1 H16
     // N65536 50.0 -> 40.9 ms, B4 H16 N16384 13.2 -> 10.7 ms; at B1 H16 N16384
     // and N32768, whose accumulators stay within twice the L2, the same).
-    int l2 = 0;
-    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
-        l2 = 128 << 20;
+    const double l2 = di.l2_bytes;
     const double acc_bytes = static_cast<double>(BH) * pb.N * D * 4.0;
     const double head_bytes = static_cast<double>(prm.group) * pb.N * D * 4.0;   // per kv head
     prm.hchunk = static_cast<int>(BHkv);
-    if (acc_bytes > 2.0 * l2)
-        prm.hchunk = static_cast<int>(
-            std::max<long long>(1, std::min<long long>(BHkv, static_cast<long long>(0.5 * l2 / head_bytes))));
-    const unsigned grid = static_cast<unsigned>(n_tiles * BHkv * hsplit);
+    if (acc_bytes > 2.0 * l2) {
+        // (a divisor of the kv head count: every chunk is whole)
+        long long hc = std::max<long long>(1, std::min<long long>(BHkv, static_cast<long long>(0.5 * l2 / head_bytes)));
+        while (BHkv % hc != 0) --hc;
+        prm.hchunk = static_cast<int>(hc);
+    }
+    // 1. Delta, LSE*log2(e), zeroed dQ accumulator.
+    bwd_pre_kernel<D><<<dim3(static_cast<unsigned>(BH), n_tiles), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(pb.o), static_cast<const __nv_bfloat16 *>(pb.dO),
+        pb.lse, pb.lse2, pb.delta, pb.dq_acc, pb.N, pb.NP);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 2. x: key tiles (heaviest first) x the chunk's kv heads x head splits;
+    // y: chunks of kv heads.
+    const long long n_chunks = BHkv / prm.hchunk;
+    const dim3 grid(static_cast<unsigned>(static_cast<long long>(n_tiles) * prm.hchunk * hsplit),
+                    static_cast<unsigned>(n_chunks));
     e = res ? launch_main<D, true>(m, prm, grid, pb.causal, stream)
             : launch_main<D, false>(m, prm, grid, pb.causal, stream);
     if (e != cudaSuccess) return e;

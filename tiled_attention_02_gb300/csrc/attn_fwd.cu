@@ -911,12 +911,11 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     // B8 H32 N8192 4.78 -> 3.78 ms, where the 152 items running at once
     // were otherwise 152 different heads; B4 H16 N16384 and B1 H16 N65536
     // the same or slightly faster).
+    DeviceInfo di;
+    if (!device_info(&di)) return cudaErrorInvalidValue;
     prm.hchunk = static_cast<int>(BH);
     {
-        int dev = 0, l2 = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
-            l2 = 128 << 20;
+        const double l2 = di.l2_bytes;
         const double head_kv = static_cast<double>(pb.N) * pb.D * 4.0 / (pb.Hq / pb.Hkv);   // per query head
         if (pb.causal && head_kv * static_cast<double>(BH) > 2.0 * l2)
             prm.hchunk = static_cast<int>(
@@ -940,13 +939,7 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     // an SM's shared memory and all of its TMEM); the residual variants one
     // block per (query tile, head).
     unsigned grid = static_cast<unsigned>(n_items);
-    if (ext == 0) {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return cudaErrorInvalidValue;
-        if (sms > 0 && n_items > sms) grid = static_cast<unsigned>(sms);
-    }
+    if (ext == 0 && n_items > di.sms) grid = static_cast<unsigned>(di.sms);
     switch (pb.D) {
     case 64: return launch_d<64>(pb.causal, ext, m, prm, grid, stream);
     case 80: return launch_d<80>(pb.causal, ext, m, prm, grid, stream);

@@ -87,4 +87,11 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdProblem &pb, int *status, cudaStream_t stream);
 cudaError_t launch_decode(const DecProblem &pb, int *status, cudaStream_t stream);
 
+// SM count and L2 size of the current device, queried once per device.
+struct DeviceInfo {
+    int sms;
+    int l2_bytes;
+};
+bool device_info(DeviceInfo *out);
+
 }  // namespace tattn
