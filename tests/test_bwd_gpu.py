@@ -103,3 +103,78 @@ def test_bwd_full_size_sampled(ta, orc):
     check_grad(dq.reshape(-1, D)[qr], ref["dq"], "dq sampled")
     check_grad(dk.reshape(-1, D)[kr], ref["dk"], "dk sampled")
     check_grad(dv.reshape(-1, D)[kr], ref["dv"], "dv sampled")
+
+
+def _bf16_close(a, b, rel=2.0 ** -7):
+    """Equal up to one bf16 rounding step (fp32 sums in another order)."""
+    a, b = a.float(), b.float()
+    return bool(((a - b).abs() <= rel * torch.maximum(a.abs(), b.abs()) + 1e-6).all())
+
+
+def test_bwd_head_chunked_order(ta, orc):
+    """Blocks in chunks of kv heads (the fp32 dQ accumulator, 537 MB, over
+    twice the L2): B=4, H=16, N=16384, D=128 causal.  Heads are independent
+    problems: dK and dV of every head equal, bit for bit, a launch on that
+    head alone (the same blocks, in the plain order), and dQ does up to the
+    order of its fp32 reduce-adds; sampled rows are checked against the
+    oracle's exact gradient."""
+    B, H, N, D = 4, 16, 16384, 128
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    assert B * H * N * D * 4 > 2 * l2, "shape must take the head-chunked order"
+    x = make_qkv(B, H, H, N, D, seed=11, with_do=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ta.attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    ta.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    for b in range(B):
+        for h in range(H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            dq1, dk1, dv1 = ta.attn_bwd(*(t[sl].contiguous() for t in (q, k, v, o, lse, do)),
+                                        causal=True)
+            assert torch.equal(dk[sl], dk1), f"dK of head ({b}, {h})"
+            assert torch.equal(dv[sl], dv1), f"dV of head ({b}, {h})"
+            assert _bf16_close(dq[sl], dq1), f"dQ of head ({b}, {h})"
+    q_rows = sample_rows(B, H, N, 256, seed=12)
+    rng = np.random.default_rng(13)
+    heads = rng.choice(B * H, size=3, replace=False)
+    k_rows = np.unique(np.concatenate(
+        [np.array([g * N, g * N + N - 1, g * N + 128]) for g in heads] +
+        [heads[rng.integers(0, 3, 120)] * N + rng.integers(0, N, 120)]))
+    ref = orc.backward_sampled(*(to_oracle(x[n]) for n in ("q", "k", "v", "do")),
+                               scale=1 / math.sqrt(D), causal=True, q_rows=q_rows, k_rows=k_rows)
+    qr, kr = torch.from_numpy(q_rows).cuda(), torch.from_numpy(k_rows).cuda()
+    check_grad(dq.reshape(-1, D)[qr], ref["dq"], "dq sampled, head-chunked")
+    check_grad(dk.reshape(-1, D)[kr], ref["dk"], "dk sampled, head-chunked")
+    check_grad(dv.reshape(-1, D)[kr], ref["dv"], "dv sampled, head-chunked")
+
+
+def test_bwd_head_chunked_grouped(ta, orc):
+    """The chunked order with grouped heads: B=2, Hq=32, Hkv=8, N=16384,
+    D=128 causal, one kv head (four query heads) per chunk.  Outputs start as
+    NaN, so every block must have written its rows; sampled rows of one kv
+    head against the oracle."""
+    B, Hq, Hkv, N, D = 2, 32, 8, 16384, 128
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    assert B * Hq * N * D * 4 > 2 * l2, "shape must take the head-chunked order"
+    x = make_qkv(B, Hq, Hkv, N, D, seed=21, with_do=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ta.attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    ta.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    q_rows = sample_rows(B, Hq, N, 256, seed=22)
+    rng = np.random.default_rng(23)
+    g = int(rng.integers(0, B * Hkv))
+    k_rows = np.unique(np.concatenate([np.array([g * N, g * N + N - 1, g * N + 128]),
+                                       g * N + rng.integers(0, N, 120)]))
+    ref = orc.backward_sampled(*(to_oracle(x[n]) for n in ("q", "k", "v", "do")),
+                               scale=1 / math.sqrt(D), causal=True, q_rows=q_rows, k_rows=k_rows)
+    qr, kr = torch.from_numpy(q_rows).cuda(), torch.from_numpy(k_rows).cuda()
+    check_grad(dq.reshape(-1, D)[qr], ref["dq"], "dq sampled, grouped head-chunked")
+    check_grad(dk.reshape(-1, D)[kr], ref["dk"], "dk sampled, grouped head-chunked")
+    check_grad(dv.reshape(-1, D)[kr], ref["dv"], "dv sampled, grouped head-chunked")

@@ -194,3 +194,33 @@ def test_parity_growing_row_max(ta, orc, D, causal):
     assert float(ref["lse"].max()) > 40.0   # the growth is really there
     check_o(o, ref["o"], f"growing max D{D} causal={causal}")
     check_lse(lse, ref["lse"], f"growing max D{D} causal={causal}")
+
+
+def test_causal_head_chunked_order(ta, orc):
+    """Causal items in chunks of heads (all heads' K/V well over twice the
+    L2): B=2, H=32, N=16384, D=128 runs its 64 heads in chunks of about half
+    the L2, the last chunk smaller.  Heads are independent problems, so every
+    row must equal, bit for bit, a launch on that head alone (one chunk, the
+    plain order); sampled rows are checked against the oracle."""
+    B, H, N, D = 2, 32, 16384, 128
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    assert B * H * N * D * 4 > 2 * l2, "shape must take the head-chunked order"
+    x = make_qkv(B, H, H, N, D, seed=7)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), device="cuda")
+    ta.attn_fwd(q, k, v, causal=True, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    for b in range(B):
+        for h in range(H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            o1, lse1 = ta.attn_fwd(q[sl].contiguous(), k[sl].contiguous(), v[sl].contiguous(),
+                                   causal=True)
+            assert torch.equal(o[sl], o1), f"O of head ({b}, {h})"
+            assert torch.equal(lse[sl], lse1), f"LSE of head ({b}, {h})"
+    rows = sample_rows(B, H, N, 256, seed=8)
+    ref = oracle_fwd(orc, x, True, 1 / math.sqrt(D), rows=rows)
+    r = torch.from_numpy(rows).cuda()
+    check_o(o.reshape(-1, D)[r], ref["o"], "head-chunked causal")
+    check_lse(lse.reshape(-1)[r], ref["lse"], "head-chunked causal")
