@@ -54,13 +54,16 @@ template <int D>
 __global__ void __launch_bounds__(256)
 bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dO,
                const float *__restrict__ lse, float *__restrict__ lse2,
-               float *__restrict__ delta, float *__restrict__ dq_acc, int N, int NP) {
+               float *__restrict__ delta, float *__restrict__ dq_acc, int N, int NP,
+               int n_tiles) {
     constexpr int kVecs = D / 8;                           // 16-byte vectors (8 bf16) per row
     constexpr int kLanesPerRow = kVecs <= 8 ? 8 : 16;      // power of two >= kVecs
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int row0 = blockIdx.y * kTile;
+    // One block per (head, row tile) on a 1D grid: B*Hq*tiles fits in 31 bits,
+    // while either factor alone may pass the 65535 limit of gridDim.y.
+    const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(n_tiles));
+    const int row0 = static_cast<int>(blockIdx.x % static_cast<unsigned>(n_tiles)) * kTile;
     const int sub = lane % kLanesPerRow;
     for (int rr = warp * kRowsPerWarp + lane / kLanesPerRow; rr < kTile; rr += 8 * kRowsPerWarp) {
         const int row = row0 + rr;
@@ -1070,12 +1073,14 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
         // (a divisor of the kv head count: every chunk is whole)
         long long hc = std::max<long long>(1, std::min<long long>(BHkv, static_cast<long long>(0.5 * l2 / head_bytes)));
         while (BHkv % hc != 0) --hc;
-        prm.hchunk = static_cast<int>(hc);
+        // The chunks are gridDim.y (at most 65535); a head count with no
+        // divisor near the target keeps the plain order.
+        if (BHkv / hc <= 65535) prm.hchunk = static_cast<int>(hc);
     }
     // 1. Delta, LSE*log2(e), zeroed dQ accumulator.
-    bwd_pre_kernel<D><<<dim3(static_cast<unsigned>(BH), n_tiles), 256, 0, stream>>>(
+    bwd_pre_kernel<D><<<static_cast<unsigned>(BH * n_tiles), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(pb.o), static_cast<const __nv_bfloat16 *>(pb.dO),
-        pb.lse, pb.lse2, pb.delta, pb.dq_acc, pb.N, pb.NP);
+        pb.lse, pb.lse2, pb.delta, pb.dq_acc, pb.N, pb.NP, n_tiles);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // 2. x: key tiles (heaviest first) x the chunk's kv heads x head splits;

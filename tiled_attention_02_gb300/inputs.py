@@ -8,6 +8,10 @@ as float32 ``randn`` (i.i.d. N(0, 1)) in a fixed order -- q, k, v, then dO
 when asked for -- and rounded to bfloat16.  A block of chained layers draws
 q, k, v (and dO) for layer 0, then layer 1, and so on, from one generator.
 The oracle widens the bfloat16 values to float exactly.
+
+Shapes too large to draw on the host use the same recipe on a seeded CUDA
+generator (``make_qkv_device``): other values than the CPU draw, and the
+oracle receives copies of the device bytes it needs.
 """
 from __future__ import annotations
 
@@ -28,6 +32,21 @@ def make_qkv(B: int, Hq: int, Hkv: int, N: int, D: int, *, seed: int = 0,
            "v": _draw(gen, (B, Hkv, N, D))}
     if with_do:
         out["do"] = _draw(gen, (B, Hq, N, D))
+    return out
+
+
+def make_qkv_device(B: int, Hq: int, Hkv: int, N: int, D: int, *, seed: int = 0,
+                    with_do: bool = False, device: str = "cuda") -> dict:
+    """As make_qkv, drawn on the device: q [B,Hq,N,D], k and v [B,Hkv,N,D]
+    (and dO like q) as bf16 tensors on ``device``."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+
+    def draw(shape):
+        return torch.randn(*shape, generator=gen, dtype=torch.float32,
+                           device=device).to(torch.bfloat16)
+    out = {"q": draw((B, Hq, N, D)), "k": draw((B, Hkv, N, D)), "v": draw((B, Hkv, N, D))}
+    if with_do:
+        out["do"] = draw((B, Hq, N, D))
     return out
 
 
