@@ -88,3 +88,28 @@ def test_decode_workspace_contents_do_not_matter(ta):
     o2, l2 = ta.attn_decode(q, k, v)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_decode_full_size(ta, orc):
+    """The decode bench line's shape, B=16, Hq=32, Hkv=8, N=16384, D=128:
+    every one of its 512 query rows against the oracle, one (batch, kv head)
+    group of query heads at a time."""
+    from tiled_attention_02_gb300.inputs import make_decode
+    B, Hq, Hkv, N, D = 16, 32, 8, 16384, 128
+    G = Hq // Hkv
+    x = make_decode(B, Hq, Hkv, N, D, seed=5)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = ta.attn_decode(q, k, v)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    ro = np.empty((B, Hq, D))
+    rl = np.empty((B, Hq))
+    for b in range(B):
+        for g in range(Hkv):
+            xg = {"q": x["q"][b:b + 1, g * G:(g + 1) * G], "k": x["k"][b:b + 1, g:g + 1],
+                  "v": x["v"][b:b + 1, g:g + 1]}
+            go, gl = oracle_decode(orc, xg, 1 / math.sqrt(D))
+            ro[b, g * G:(g + 1) * G] = go[0]
+            rl[b, g * G:(g + 1) * G] = gl[0]
+    check_o(o, ro, "decode full size")
+    check_lse(lse, rl, "decode full size")
