@@ -256,19 +256,30 @@ def backward(q, k, v, dO, *, scale: float, causal: bool, window=None, bias=None,
     return out
 
 
-def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows, window=None):
+def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows, window=None,
+                     bias=None, grad_in=None):
     """dQ at flat query rows ``q_rows`` and dK/dV at flat key rows ``k_rows``.
+
+    bias and grad_in: as for ``backward`` ([B,Hq,N,N] or None), read only at
+    the query rows involved, so an array filled at those rows alone serves.
 
     Key row flat index is ``(b*Hkv + g)*N + j``.  The statistics LSE and Delta
     are computed by the oracle's own forward pass over every query row of the
     heads involved (a key row needs all the query rows that attend to it).
-    Returns dict with dq [len(q_rows), D], dk and dv [len(k_rows), D].
+    Returns dict with dq [len(q_rows), D], dk and dv [len(k_rows), D], and
+    dlogits [len(q_rows), N]: the total logit gradient dS of those rows (0 at
+    keys outside J_i), the grad_in of the layer below in a residual chain.
     """
     lib = _load()
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     B, Hq, Hkv, N, D = _shapes(q, k, v)
     w = _window(causal, window)
     group = Hq // Hkv
+    bias = None if bias is None else _f64(bias)
+    grad_in = None if grad_in is None else _f64(grad_in)
+    for name, t in (("bias", bias), ("grad_in", grad_in)):
+        if t is not None and t.shape != (B, Hq, N, N):
+            raise ValueError(f"{name} must be [B,Hq,N,N]")
     qr, nq = _rows(q_rows, B * Hq * N)
     kr, nk = _rows(k_rows, B * Hkv * N)
     # Query rows whose statistics are needed.
@@ -291,18 +302,20 @@ def backward_sampled(q, k, v, dO, *, scale: float, causal: bool, q_rows, k_rows,
     lse = np.zeros((B * Hq * N,), dtype=np.float64)
     dlt = np.zeros((B * Hq * N,), dtype=np.float64)
     if stat_rows.size:
-        fw = forward(q, k, v, scale=scale, causal=causal, rows=stat_rows, window=window)
+        fw = forward(q, k, v, scale=scale, causal=causal, rows=stat_rows, window=window,
+                     bias=bias)
         lse[stat_rows] = fw["lse"]
         dlt[stat_rows] = delta(dO, fw["o"], stat_rows)
     dq = np.empty((nq, D), dtype=np.float64)
     dk = np.empty((nk, D), dtype=np.float64)
     dv = np.empty((nk, D), dtype=np.float64)
+    dl = np.empty((nq, N), dtype=np.float64)
     if nq:
-        lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), None, None, B, Hq,
-                            Hkv, N, D, float(scale), int(bool(causal)), w, _p(qr), nq, _p(dq),
-                            None)
+        lib.orc_bwd_dq_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), _p(bias),
+                            _p(grad_in), B, Hq, Hkv, N, D, float(scale), int(bool(causal)), w,
+                            _p(qr), nq, _p(dq), _p(dl))
     if nk:
-        lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), None, None, B, Hq,
-                             Hkv, N, D, float(scale), int(bool(causal)), w, _p(kr), nk, _p(dk),
-                             _p(dv))
-    return {"dq": dq, "dk": dk, "dv": dv}
+        lib.orc_bwd_dkv_rows(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), _p(bias),
+                             _p(grad_in), B, Hq, Hkv, N, D, float(scale), int(bool(causal)), w,
+                             _p(kr), nk, _p(dk), _p(dv))
+    return {"dq": dq, "dk": dk, "dv": dv, "dlogits": dl}

@@ -371,6 +371,28 @@ def test_backward_sampled_equals_full(orc):
     np.testing.assert_allclose(part["dv"], full["dv"].reshape(-1, D)[kr], rtol=0, atol=1e-14)
 
 
+def test_backward_sampled_with_residual_equals_full(orc):
+    """Sampled rows with a logit bias and an incoming logit gradient (filled
+    only at the sampled query rows' heads, as a full-size test does) match
+    the full residual backward, dlogits rows included."""
+    B, Hq, Hkv, N, D = 1, 4, 2, 8, 3
+    q, k, v, do = rand(B, Hq, N, D), rand(B, Hkv, N, D), rand(B, Hkv, N, D), rand(B, Hq, N, D)
+    bias, gin = rand(B, Hq, N, N), rand(B, Hq, N, N)
+    full = orc.backward(q, k, v, do, scale=0.5, causal=True, bias=bias, grad_in=gin)
+    qr = np.array([0, 3, 9, 31])
+    part = orc.backward_sampled(q, k, v, do, scale=0.5, causal=True, q_rows=qr, k_rows=[],
+                                bias=bias, grad_in=gin)
+    np.testing.assert_allclose(part["dq"], full["dq"].reshape(-1, D)[qr], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(part["dlogits"], full["dlogits"].reshape(-1, N)[qr], rtol=0,
+                               atol=1e-14)
+    # only the sampled rows of bias and grad_in are read
+    sb, sg = np.full_like(bias, np.nan), np.full_like(gin, np.nan)
+    sb.reshape(-1, N)[qr], sg.reshape(-1, N)[qr] = bias.reshape(-1, N)[qr], gin.reshape(-1, N)[qr]
+    part2 = orc.backward_sampled(q, k, v, do, scale=0.5, causal=True, q_rows=qr, k_rows=[],
+                                 bias=sb, grad_in=sg)
+    np.testing.assert_array_equal(part2["dq"], part["dq"])
+
+
 def test_backward_zero_output_grad(orc):
     B, H, N, D = 1, 2, 5, 3
     q, k, v = rand(B, H, N, D), rand(B, H, N, D), rand(B, H, N, D)

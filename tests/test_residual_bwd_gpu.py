@@ -133,3 +133,65 @@ def test_residual_chain_backward(ta, orc):
         check_grad(dk, r["dk"], f"chain dk {i}")
         check_grad(dv, r["dv"], f"chain dv {i}")
         g_in = r.get("dlogits")
+
+
+def test_residual_chain_backward_full_size_sampled(ta, orc):
+    """The block-residual training step at full size: 4 layers, B=1, Hq=20,
+    Hkv=4, N=4096, D=128, causal, forward then backward through the block
+    with one gradient buffer passed down in place.  Row i of a layer's dQ
+    and of its outgoing logit gradient depends only on row i of its bias
+    (the layer below's logits) and of the gradient arriving from the layer
+    above, so the oracle follows 256 sampled query rows through the whole
+    block, up and back down."""
+    from helpers import sample_rows
+    B, Hq, Hkv, N, D, L = 1, 20, 4, 4096, 128, 4
+    scale = 1 / math.sqrt(D)
+    layers = make_chain(B, Hq, Hkv, N, D, layers=L, seed=9, with_do=True)
+    dev = [{n: x[n].cuda() for n in ("q", "k", "v", "do")} for x in layers]
+    S = [torch.empty((B, Hq, N, N), device="cuda") for _ in range(L - 1)]
+    fw = []
+    for i, x in enumerate(dev):
+        fw.append(ta.attn_fwd(x["q"], x["k"], x["v"], S[i - 1] if i > 0 else None, causal=True,
+                              emit_logits=S[i] if i < L - 1 else None))
+    gbuf = torch.empty((B, Hq, N, N), device="cuda")
+    dq = [None] * L
+    for i in reversed(range(L)):
+        x, (o, lse) = dev[i], fw[i]
+        dq[i], dk, dv = ta.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=True,
+                                    bias=S[i - 1] if i > 0 else None,
+                                    grad_in=gbuf if i < L - 1 else None,
+                                    grad_out=gbuf if i > 0 else None)
+        assert torch.isfinite(dk.float()).all() and torch.isfinite(dv.float()).all()
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    rows = sample_rows(B, Hq, N, 256, seed=10)
+    rows_t = torch.from_numpy(rows).cuda()
+    ox = [{n: to_oracle(x[n]) for n in ("q", "k", "v", "do")} for x in layers]
+    # up: the sampled rows' logits of layers 0..L-2, each the next one's bias
+    bias_rows, prev = [None], None
+    for i in range(L - 1):
+        f = orc.forward(ox[i]["q"], ox[i]["k"], ox[i]["v"], scale=scale, causal=True, rows=rows,
+                        bias=prev, emit_logits=True)
+        prev = np.nan_to_num(f["logits"])
+        bias_rows.append(prev)
+
+    def at_rows(r):
+        """A [B,Hq,N,N] array holding r at the sampled rows (zero pages elsewhere)."""
+        if r is None:
+            return None
+        full = np.zeros((B, Hq, N, N))
+        full.reshape(-1, N)[rows] = r
+        return full
+    # down: dQ and the outgoing logit gradient of the same rows
+    g_rows = None
+    for i in reversed(range(L)):
+        r = orc.backward_sampled(ox[i]["q"], ox[i]["k"], ox[i]["v"], ox[i]["do"], scale=scale,
+                                 causal=True, q_rows=rows, k_rows=[], bias=at_rows(bias_rows[i]),
+                                 grad_in=at_rows(g_rows))
+        check_grad(dq[i].reshape(-1, D)[rows_t], r["dq"], f"chain dq {i} sampled")
+        g_rows = r["dlogits"]
+        if i == 1:   # the buffer holds layer 1's outgoing gradient at the end
+            got = gbuf.reshape(-1, N)[rows_t].cpu().numpy().astype(np.float64)
+            keep = np.arange(N)[None, :] <= (rows % N)[:, None]
+            err = np.abs(got - g_rows)[keep].max()
+            assert err <= DLOGIT_ABS, f"layer 1 logit gradient max-abs {err:.3e}"
