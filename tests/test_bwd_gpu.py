@@ -85,21 +85,40 @@ def test_bwd_workspace_contents_do_not_matter(ta):
         assert (u.float() - w.float()).abs().max().item() < 1e-2
 
 
-def test_bwd_full_size_sampled(ta, orc):
-    """B=1, H=16, N=16384, D=128, causal: 256 sampled query rows (dQ) and
-    256 sampled key rows (dK, dV) against the oracle's exact gradient."""
-    B, H, N, D = 1, 16, 16384, 128
+FULL_SIZE = [
+    # D, window: the default step's shape (B=1, H=16, N=16384, causal) at each head
+    # dim the bench times, and its 4096-key sliding window
+    (128, None), (80, None), (96, None), (128, 4096),
+]
+
+
+@pytest.mark.parametrize("D,window", FULL_SIZE,
+                         ids=[f"D{d}" + (f"W{w}" if w else "") for d, w in FULL_SIZE])
+def test_bwd_full_size_sampled(ta, orc, D, window):
+    """B=1, H=16, N=16384, causal: O and LSE at 256 sampled query rows, dQ
+    at the same rows and dK, dV at 256 sampled key rows against the oracle's
+    exact values."""
+    from helpers import check_lse, check_o
+    B, H, N = 1, 16, 16384
     x = make_qkv(B, H, H, N, D, seed=0, with_do=True)
-    dq, dk, dv = gpu_fwd_bwd(ta, x, True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ta.attn_fwd(q, k, v, causal=True, window=window)
+    dq, dk, dv = ta.attn_bwd(q, k, v, o, lse, do, causal=True, window=window)
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
     q_rows = sample_rows(B, H, N, 256, seed=3)
     rng = np.random.default_rng(4)
     heads = rng.choice(H, size=4, replace=False)
     k_rows = np.unique(np.concatenate([
         np.array([h * N, h * N + N - 1, h * N + 127, h * N + 128]) for h in heads] + [
         heads[rng.integers(0, 4, 240)] * N + rng.integers(0, N, 240)]))
-    ref = orc.backward_sampled(*(to_oracle(x[n]) for n in ("q", "k", "v", "do")),
-                               scale=1 / math.sqrt(D), causal=True, q_rows=q_rows, k_rows=k_rows)
+    ox = [to_oracle(x[n]) for n in ("q", "k", "v", "do")]
+    ref = orc.backward_sampled(*ox, scale=1 / math.sqrt(D), causal=True, window=window,
+                               q_rows=q_rows, k_rows=k_rows)
+    fw = orc.forward(*ox[:3], scale=1 / math.sqrt(D), causal=True, window=window, rows=q_rows)
     qr, kr = torch.from_numpy(q_rows).cuda(), torch.from_numpy(k_rows).cuda()
+    check_o(o.reshape(-1, D)[qr], fw["o"], "O sampled")
+    check_lse(lse.reshape(-1)[qr], fw["lse"], "LSE sampled")
     check_grad(dq.reshape(-1, D)[qr], ref["dq"], "dq sampled")
     check_grad(dk.reshape(-1, D)[kr], ref["dk"], "dk sampled")
     check_grad(dv.reshape(-1, D)[kr], ref["dv"], "dv sampled")
