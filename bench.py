@@ -574,7 +574,7 @@ def run_ours(args):
         phases_b, _, dev_inputs_b, results_b = build_workload()
         sets = [(phases, dev_inputs, results), (phases_b, dev_inputs_b, results_b)]
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        n_e2e = max(4, min(args.steps, 20))
+        n_e2e = max(4, min(args.steps, 50))
 
         def serial_step():
             for d, h in zip(dev_inputs, pinned):
