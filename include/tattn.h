@@ -49,7 +49,9 @@
  *    the launches are queued.
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns ATTN_ERR_INVALID (or ATTN_ERR_UNSUPPORTED for a valid
- *    but unimplemented case) and touches no memory.  A launch failure
+ *    but unimplemented case) and touches no memory.  Sizes are limited by
+ *    B*Hq*ceil(N/128) <= 2^31 - 1 (ATTN_ERR_UNSUPPORTED past it); within
+ *    that bound every launch fits the grid limits.  A launch failure
  *    returns ATTN_ERR_CUDA.  Faults found on the device (a pipeline wait
  *    that ran out of time, a failed device-side check) do not trap: the
  *    kernel records a code in the status word and returns; read it with
