@@ -62,6 +62,9 @@ def fwd(ta, **kw):
     (dict(D=72), 2), (dict(D=112), 2), (dict(D=256), 2), (dict(D=0), 1), (dict(D=-64), 1),
     (dict(Hkv=3), 1), (dict(Hkv=0), 1), (dict(B=-1), 1), (dict(N=-5), 1),
     (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    # B*Hq*ceil(N/128) = 2^31, one past the bound: by heads and by length
+    (dict(B=1 << 16, Hq=1 << 15, Hkv=1 << 15, N=128), 2),
+    (dict(B=1, Hq=256, Hkv=256, N=1 << 30), 2),
 ])
 def test_fwd_rejects_bad_arguments(ta, kw, code):
     assert fwd(ta, **kw) == code
@@ -82,6 +85,8 @@ def bwd(ta, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(lse=None), 1), (dict(do=None), 1), (dict(ws=None), 1), (dict(dk=A + 2), 1),
     (dict(ws=A + 16), 1), (dict(ws_bytes=1000), 1), (dict(D=32), 2), (dict(Hkv=3), 1),
+    (dict(B=1 << 16, Hq=1 << 15, Hkv=1 << 15, N=128), 2),
+    (dict(B=1, Hq=256, Hkv=256, N=1 << 30), 2),
 ])
 def test_bwd_rejects_bad_arguments(ta, kw, code):
     assert bwd(ta, **kw) == code
