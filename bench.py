@@ -95,20 +95,32 @@ DEC_SOURCES = ["tiled_attention_02_gb300/csrc/attn_decode.cu",
                "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
 
 
-def profiled_traffic(kernel_tag, digest, units):
-    """DRAM bytes per launch from the committed ncu summary for this kernel,
-    scaled to `units` (query-tile x kv-tile pairs) when it was captured on a
-    smaller case; None if absent or if the kernel source changed since."""
+def profiled(kernel_tag, digest, units):
+    """What the committed ncu summary ``profiles/<kernel_tag>.md`` says about
+    this kernel, if it was captured on the same kernel source (digest):
+    DRAM bytes per launch (``traffic``), scaled to `units` (query-tile x
+    kv-tile pairs) when the capture ran a smaller case, and the tensor
+    pipe's active cycles in percent of peak (``tensor_pipe_active_pct``, as
+    captured).  Empty when absent or stale."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     if not os.path.exists(path):
-        return None
+        return {}
     text = open(path).read()
     m_d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m_d or m_d.group(1) != digest:
+        return {}
+    out = {"profile": f"profiles/{kernel_tag}.md"}
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_u = re.search(r"units_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_d and m_b and m_u) or m_d.group(1) != digest:
-        return None
-    return float(m_b.group(1)) * units / float(m_u.group(1))
+    if m_b and m_u:
+        cap_units = float(m_u.group(1))
+        out["traffic"] = float(m_b.group(1)) * units / cap_units
+        out["traffic_basis"] = ("measured at this size" if cap_units == units else
+                                f"scaled by units from a capture of {cap_units:.0f} units")
+    m_t = re.search(r"tensor_pipe_active_pct:\s*([0-9.eE+]+)", text)
+    if m_t:
+        out["tensor_pipe_active_pct"] = float(m_t.group(1))
+    return out
 
 
 # ----------------------------------------------------------------- clocks
@@ -270,13 +282,34 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_block(world),
+            "config": line_config(WORKLOAD, world, wants_flush("auto", workload_bytes(WORKLOAD)),
+                                  workload_bytes(WORKLOAD)),
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                              "sample": s["desc"]},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def line_config(W, world, do_flush, bytes_per_step):
+    """The JSON line's `config`, the same for both arms."""
+    kind = W.get("kind", "fwd_bwd")
+    return dict(config_block(world, W),
+                step={"fwd_bwd": "forward + backward", "fwd": "forward",
+                      "decode": "one decode step (stream-K over one block per SM, then merge)",
+                      "chain_train": "four chained layers forward, then backward "
+                                     "through the block (fp32 residual and gradient)",
+                      "chain": "four chained forward layers, fp32 residual in place"}[kind],
+                l2=l2_note(do_flush, bytes_per_step))
+
+
+def workload_bytes(W):
+    """Algorithmic bytes of one step of W (as the GPU arm counts them)."""
+    B, Hq, Hkv, N, D = W["B"], W["Hq"], W["Hkv"], W["N"], W["D"]
+    io = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+    bw = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+    return io + (bw if W.get("kind", "fwd_bwd") == "fwd_bwd" else 0)
 
 
 def config_block(world, W=None):
@@ -344,171 +377,337 @@ def chain_layer_bytes(W, layer):
 
 # ---------------------------------------------------------------- GPU arm
 
+def build_workload(W, ta, dev, rank, sh):
+    """One independent set of device buffers for workload W and the phases
+    that run on them: (phases, host inputs, device inputs, results), where a
+    phase is (label, fn, flops, algorithmic bytes) and a step runs every
+    phase in order."""
+    import torch
+    from tiled_attention_02_gb300.inputs import make_chain, make_qkv
+    kind = W.get("kind", "fwd_bwd")
+    B, Hq, Hkv, N, D, causal = W["B"], W["Hq"], W["Hkv"], W["N"], W["D"], W["causal"]
+    scale = 1.0 / math.sqrt(D)
+    phases = []
+    host_inputs, dev_inputs, results = [], [], []
+    if kind == "decode":
+        from tiled_attention_02_gb300.inputs import make_decode
+        x = make_decode(B, Hq, Hkv, N, D, seed=rank)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(ta.attn_decode_workspace_size(B, Hq, Hkv, N, D), 256),
+                         dtype=torch.uint8, device=dev)
+
+        def dec():
+            s = ta.raw_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, Hq, Hkv, N, D, scale, ws.data_ptr(),
+                                   ws.numel(), sh)
+            assert s == 0, s
+        # algorithmic bytes: the K/V cache once, the query rows, O and LSE
+        dec_bytes = 2 * (B * Hkv * N * D) * 2 + 2 * (B * Hq * D) * 2 + B * Hq * 4
+        phases.append(("decode", dec, 4.0 * B * Hq * N * D, dec_bytes))
+        # The K/V cache is state that stays on the device across decode
+        # steps; a step's input is its query rows.
+        host_inputs += [x["q"]]
+        dev_inputs += [q]
+        results = [o]
+    elif kind == "chain_train":
+        # 4-layer block, forward then backward: every layer keeps its emitted
+        # logits (the next layer's bias, needed again by the backward), and
+        # one fp32 buffer carries the logit gradient down the block in place.
+        L = W["layers"]
+        layers = make_chain(B, Hq, Hkv, N, D, layers=L, seed=rank, with_do=True)
+        dl = [{n: x[n].to(dev) for n in ("q", "k", "v", "do")} for x in layers]
+        outs = [(torch.empty_like(x["q"]),
+                 torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
+        S = [torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev) for _ in range(L - 1)]
+        gbuf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
+        grads = [(torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
+                 for x in dl]
+        ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+                         dtype=torch.uint8, device=dev)
+        kept = B * Hq * (N * (N + 1) // 2 if causal else N * N) * 4
+        for i in range(L):
+            def layer_f(i=i):
+                x, (o, lse) = dl[i], outs[i]
+                st = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                     S[i - 1].data_ptr() if i > 0 else None, o.data_ptr(),
+                                     lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                     S[i].data_ptr() if i < L - 1 else None, sh)
+                assert st == 0, st
+            phases.append((f"fwd{i}", layer_f, attn_flops(B, Hq, N, D, causal),
+                           chain_layer_bytes(W, i)))
+        io_b = 5 * (B * Hq * N * D) * 2 + 2 * 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+        for i in reversed(range(L)):
+            def layer_b(i=i):
+                x, (o, lse) = dl[i], outs[i]
+                dq, dk, dv = grads[i]
+                st = ta.raw_attn_bwd_residual(
+                    x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
+                    lse.data_ptr(), x["do"].data_ptr(), S[i - 1].data_ptr() if i > 0 else None,
+                    gbuf.data_ptr() if i < L - 1 else None, dq.data_ptr(), dk.data_ptr(),
+                    dv.data_ptr(), gbuf.data_ptr() if i > 0 else None, B, Hq, Hkv, N, D, scale,
+                    causal, ws.data_ptr(), ws.numel(), sh)
+                assert st == 0, st
+            by = io_b + kept * ((i > 0) + (i < L - 1) + (i > 0))
+            phases.append((f"bwd{i}", layer_b, bwd_flops(B, Hq, N, D, causal), by))
+        for i, x in enumerate(layers):
+            for n in ("q", "k", "v", "do"):
+                host_inputs.append(x[n])
+                dev_inputs.append(dl[i][n])
+        results = [grads[0][0]]
+    elif kind == "chain":
+        layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
+        dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
+        outs = [(torch.empty_like(x["q"]),
+                 torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
+        buf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
+        L = W["layers"]
+        for i in range(L):
+            def layer(i=i):
+                x, (o, lse) = dl[i], outs[i]
+                s = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                    buf.data_ptr() if i > 0 else None, o.data_ptr(),
+                                    lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
+                                    buf.data_ptr() if i < L - 1 else None, sh)
+                assert s == 0, s
+            phases.append((f"layer{i}", layer, attn_flops(B, Hq, N, D, causal),
+                           chain_layer_bytes(W, i)))
+        for i, x in enumerate(layers):
+            for n in ("q", "k", "v"):
+                host_inputs.append(x[n])
+                dev_inputs.append(dl[i][n])
+        results = [outs[-1][0]]
+    else:
+        x = make_qkv(B, Hq, Hkv, N, D, seed=rank, with_do=(kind == "fwd_bwd"))
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+
+        window = W.get("window")
+
+        def fwd():
+            if window:
+                s = ta.raw_attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
+                                           o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                           window, None, sh)
+            else:
+                s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
+                                    o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                    causal, None, sh)
+            assert s == 0, s
+        io_bytes = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+        phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal, window), io_bytes))
+        host_inputs += [x["q"], x["k"], x["v"]]
+        dev_inputs += [q, k, v]
+        results = [o]
+        if kind == "fwd_bwd":
+            do = x["do"].to(dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
+                             dtype=torch.uint8, device=dev)
+
+            def bwd():
+                if window:
+                    s = ta.raw_attn_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B,
+                                               Hq, Hkv, N, D, scale, window, ws.data_ptr(),
+                                               ws.numel(), sh)
+                else:
+                    s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                        dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, D, scale,
+                                        causal, ws.data_ptr(), ws.numel(), sh)
+                assert s == 0, s
+            bwd_bytes = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
+            phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal, window), bwd_bytes))
+            host_inputs.append(x["do"])
+            dev_inputs.append(do)
+            results = [dq, dk, dv]
+    return phases, host_inputs, dev_inputs, results
+
+
+LAUNCHES = {"fwd": 1, "bwd": 3, "decode": 2, **{f"bwd{i}": 3 for i in range(8)}}
+
+
+def pct_stats(xs):
+    """median / p90 / min of a list of times, as the pages' CUDA-event bench
+    template reports them (p90 by nearest rank)."""
+    ys = sorted(xs)
+    return {"median": statistics.median(ys), "p90": ys[max(0, math.ceil(0.9 * len(ys)) - 1)],
+            "min": ys[0]}
+
+
+def wants_flush(l2_mode, bytes_per_step):
+    """Between timed steps either flush L2 (write a buffer larger than it) or
+    rely on a step's own traffic being more than twice the L2, which leaves
+    nothing of the previous step resident."""
+    return l2_mode == "flush" or (l2_mode == "auto" and bytes_per_step <= 2 * L2_BYTES)
+
+
+def l2_note(do_flush, bytes_per_step):
+    return (f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)" if do_flush else
+            f"no flush: inputs larger than L2 (a step moves {bytes_per_step / 2**20:.0f} MB, "
+            f"over twice the {L2_BYTES >> 20} MB L2)")
+
+
+def time_steps(phases, stream, n, do_flush, flush):
+    """n steps, each phase bracketed by CUDA events on the launching stream;
+    returns per-step lists of per-phase milliseconds."""
+    import torch
+    nph = len(phases)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n)]
+    for i in range(n):
+        if do_flush:
+            flush.fill_(float(i))   # untimed: evicts the previous step's data from L2
+        ev[i][0].record(stream)
+        for j, (_, fn, _, _) in enumerate(phases):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    return [[e[j].elapsed_time(e[j + 1]) for j in range(nph)] for e in ev]
+
+
+def kernel_entries(W, phases, ph_ms, pk):
+    """Roofline entry per phase: achieved rate from the CUDA-event time
+    (`ph_ms`: milliseconds per launch of each phase) against the measured
+    peak, with DRAM traffic and tensor-pipe activity from the committed ncu
+    summary of the same kernel source."""
+    kind = W.get("kind", "fwd_bwd")
+    B, Hq, Hkv, N, D, causal = W["B"], W["Hq"], W["Hkv"], W["N"], W["D"], W["causal"]
+    units = tile_pairs(B, Hq, N, causal, W.get("window"))   # 128x128 tile pairs
+    tag = (f"{'causal' if causal else 'noncausal'}_B{B}_H{Hq}_N{N}_D{D}"
+           + (f"_W{W['window']}" if W.get("window") else ""))
+    kernels = {}
+    for (lbl, _, fl, by), avg in zip(phases, ph_ms):
+        if kind == "decode":
+            dg = source_digest(DEC_SOURCES)
+            ach = by / (avg * 1e-3) / 1e9
+            kernels[lbl] = dict({"kernel": f"decode_split_kernel<{D}> + decode_merge_kernel",
+                                 "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                                 "unit": "GB/s", "frac": ach / pk["hbm_gbs"]},
+                                **profiled(f"decode_split_kernel_{W['name']}", dg, B * Hkv * N),
+                                bytes_per_launch=by, flops_per_launch=fl,
+                                tflops=fl / (avg * 1e-3) / 1e12, avg_launch_ms=avg,
+                                launches_timed=2, source_digest=dg)
+            continue
+        if kind in ("chain", "chain_train"):
+            is_b = lbl.startswith("bwd")
+            dg = source_digest(BWD_SOURCES if is_b else FWD_SOURCES)
+            ach = by / (avg * 1e-3) / 1e9
+            if is_b:
+                prof = profiled(f"bwd_main_kernel_residual_chain_train_B{B}_H{Hq}_N{N}_D{D}", dg,
+                                units) if lbl in ("bwd1", "bwd2") else {}
+            else:
+                mid = lbl in ("fwd1", "fwd2", "layer1", "layer2")
+                prof = profiled(f"fwd_kernel_chain_{tag}", dg, units) if mid else {}
+            kernels[lbl] = dict({"kernel": (f"bwd_main_kernel<{D},causal,residual> (+pre, dQ "
+                                            f"convert)" if is_b else
+                                            f"fwd_kernel<{D},causal,bias/emit>"),
+                                 "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                                 "unit": "GB/s", "frac": ach / pk["hbm_gbs"]},
+                                **prof, bytes_per_launch=by, flops_per_launch=fl,
+                                tflops=fl / (avg * 1e-3) / 1e12, avg_launch_ms=avg,
+                                launches_timed=3 if is_b else 1, source_digest=dg)
+            continue
+        is_bwd = lbl == "bwd"
+        dg = source_digest(BWD_SOURCES if is_bwd else FWD_SOURCES)
+        ach = fl / (avg * 1e-3) / 1e12
+        kname = "bwd_main_kernel" if is_bwd else "fwd_kernel"
+        kernels[lbl] = dict({"kernel": f"{kname}<{D},{'causal' if causal else 'noncausal'}>",
+                             "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                             "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"]},
+                            **profiled(f"{kname}_{tag}", dg, units),
+                            flops_per_launch=fl, units_per_launch=units, avg_launch_ms=avg,
+                            launches_timed=3 if is_bwd else 1, source_digest=dg)
+        if is_bwd:
+            kernels[lbl]["timing_note"] = ("CUDA events around attn_bwd: preprocess + main + "
+                                           "dQ convert; the main kernel dominates (ncu launch "
+                                           "list)")
+    return kernels
+
+
+# The other configurations, timed after the default line in the same run
+# with the pages' CUDA-event template: 20 warm-up and 100 timed iterations,
+# median / p90 / min (blog.ans20xx.com day26, "CUDA event 计时模板").
+CONFIG_SET = (("C1", "tiny"), ("C2", "noncausal_fwd"), ("C3", "causal_fwd_d64"),
+              ("C4", "residual_chain"), ("C4_train", "residual_chain_train"))
+# The pages' own figure for C3's shape: flash-attn v2 forward on an H100-SXM,
+# 11.9 ms median, counted 4*B*H*S^2*D without the causal halving
+# (blog.ans20xx.com day26, "报告格式").
+PAGES_C3_FA2_H100 = {"ms": 11.9, "tflops_unhalved": 11.57, "hardware": "H100-SXM-80GB"}
+
+
+def time_config(W, ta, dev, sh, stream, flush, l2_mode, pk, n_warm=20, n_iter=100):
+    phases, _, _, _ = build_workload(W, ta, dev, 0, sh)
+    kind = W.get("kind", "fwd_bwd")
+    bytes_step = sum(ph[3] for ph in phases)
+    flops_step = sum(ph[2] for ph in phases)
+    do_flush = wants_flush(l2_mode, bytes_step)
+    for _ in range(n_warm):
+        for _, fn, _, _ in phases:
+            fn()
+    import torch
+    torch.cuda.synchronize()
+    assert ta.attn_last_device_status() == 0
+    per = time_steps(phases, stream, n_iter, do_flush, flush)
+    assert ta.attn_last_device_status() == 0
+    step_ms = [sum(p) for p in per]
+    st = pct_stats(step_ms)
+    ph_med = [statistics.median(p[j] for p in per) for j in range(len(phases))]
+    out = {"workload": W["name"], "ms": st, "iters": n_iter, "warmup": n_warm,
+           "l2": l2_note(do_flush, bytes_step),
+           "gpu_launches_per_iter": sum(LAUNCHES.get(lbl, 1) for lbl, *_ in phases)}
+    kernels = kernel_entries(W, phases, ph_med, pk)
+    if W["name"].startswith("tiny"):
+        out["us"] = {k: 1e3 * v for k, v in st.items()}
+        out["bound"] = "launch latency (4.19 MFLOP; a rate is not meaningful)"
+        return out
+    out["tflops"] = flops_step / (st["median"] * 1e-3) / 1e12
+    if kind in ("chain", "chain_train"):
+        out["gbs"] = bytes_step / (st["median"] * 1e-3) / 1e9
+        out["bound"] = "hbm"
+        out["frac"] = out["gbs"] / pk["hbm_gbs"]
+        out["peak"] = pk["hbm_gbs"]
+        out["phases"] = {lbl: {"ms_median": kernels[lbl]["avg_launch_ms"],
+                               "gbs": kernels[lbl]["achieved"], "frac": kernels[lbl]["frac"],
+                               **{k: kernels[lbl][k] for k in ("traffic",
+                                                               "tensor_pipe_active_pct")
+                                  if kernels[lbl].get(k) is not None}}
+                         for lbl in kernels}
+    else:
+        k0 = kernels["fwd"]
+        out.update({"bound": "tensor", "frac": k0["frac"], "peak": pk["bf16_tflops"],
+                    "kernel": k0["kernel"]})
+        for key in ("traffic", "tensor_pipe_active_pct", "profile"):
+            if k0.get(key) is not None:
+                out[key] = k0[key]
+        if W["causal"]:
+            out["tflops_unhalved"] = 2 * out["tflops"]
+        if W["name"] == EXTRA_WORKLOADS["causal_fwd_d64"]["name"]:
+            out["pages_context"] = dict(PAGES_C3_FA2_H100,
+                                        note="another machine: context, not a target")
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup(want_cuda=True)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import tiled_attention_02_gb300 as ta
-    from tiled_attention_02_gb300.inputs import make_chain, make_qkv
     ta.build()
     W = WORKLOAD if args.workload == "step" else EXTRA_WORKLOADS[args.workload]
     kind = W.get("kind", "fwd_bwd")
-    B, Hq, Hkv, N, D, causal = W["B"], W["Hq"], W["Hkv"], W["N"], W["D"], W["causal"]
-    scale = 1.0 / math.sqrt(D)
+    B, Hq, N, D, causal = W["B"], W["Hq"], W["N"], W["D"], W["causal"]
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    pk = peaks()
 
-    def build_workload():
-        """One independent set of device buffers and the phases that run on
-        them: (phases, host inputs, device inputs, results)."""
-        # phases: list of (label, fn, flops, algorithmic bytes) run in order per step
-        phases = []
-        host_inputs, dev_inputs, results = [], [], []
-        if kind == "decode":
-            from tiled_attention_02_gb300.inputs import make_decode
-            x = make_decode(B, Hq, Hkv, N, D, seed=rank)
-            q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-            o = torch.empty_like(q)
-            lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-            ws = torch.empty(max(ta.attn_decode_workspace_size(B, Hq, Hkv, N, D), 256),
-                             dtype=torch.uint8, device=dev)
-
-            def dec():
-                s = ta.raw_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                       lse.data_ptr(), B, Hq, Hkv, N, D, scale, ws.data_ptr(),
-                                       ws.numel(), sh)
-                assert s == 0, s
-            # algorithmic bytes: the K/V cache once, the query rows, O and LSE
-            dec_bytes = 2 * (B * Hkv * N * D) * 2 + 2 * (B * Hq * D) * 2 + B * Hq * 4
-            phases.append(("decode", dec, 4.0 * B * Hq * N * D, dec_bytes))
-            # The K/V cache is state that stays on the device across decode
-            # steps; a step's input is its query rows.
-            host_inputs += [x["q"]]
-            dev_inputs += [q]
-            results = [o]
-        elif kind == "chain_train":
-            # 4-layer block, forward then backward: every layer keeps its emitted
-            # logits (the next layer's bias, needed again by the backward), and
-            # one fp32 buffer carries the logit gradient down the block in place.
-            L = W["layers"]
-            layers = make_chain(B, Hq, Hkv, N, D, layers=L, seed=rank, with_do=True)
-            dl = [{n: x[n].to(dev) for n in ("q", "k", "v", "do")} for x in layers]
-            outs = [(torch.empty_like(x["q"]),
-                     torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
-            S = [torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev) for _ in range(L - 1)]
-            gbuf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
-            grads = [(torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
-                     for x in dl]
-            ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
-                             dtype=torch.uint8, device=dev)
-            kept = B * Hq * (N * (N + 1) // 2 if causal else N * N) * 4
-            for i in range(L):
-                def layer_f(i=i):
-                    x, (o, lse) = dl[i], outs[i]
-                    st = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
-                                         S[i - 1].data_ptr() if i > 0 else None, o.data_ptr(),
-                                         lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
-                                         S[i].data_ptr() if i < L - 1 else None, sh)
-                    assert st == 0, st
-                phases.append((f"fwd{i}", layer_f, attn_flops(B, Hq, N, D, causal),
-                               chain_layer_bytes(W, i)))
-            io_b = 5 * (B * Hq * N * D) * 2 + 2 * 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-            for i in reversed(range(L)):
-                def layer_b(i=i):
-                    x, (o, lse) = dl[i], outs[i]
-                    dq, dk, dv = grads[i]
-                    st = ta.raw_attn_bwd_residual(
-                        x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
-                        lse.data_ptr(), x["do"].data_ptr(), S[i - 1].data_ptr() if i > 0 else None,
-                        gbuf.data_ptr() if i < L - 1 else None, dq.data_ptr(), dk.data_ptr(),
-                        dv.data_ptr(), gbuf.data_ptr() if i > 0 else None, B, Hq, Hkv, N, D, scale,
-                        causal, ws.data_ptr(), ws.numel(), sh)
-                    assert st == 0, st
-                by = io_b + kept * ((i > 0) + (i < L - 1) + (i > 0))
-                phases.append((f"bwd{i}", layer_b, bwd_flops(B, Hq, N, D, causal), by))
-            for i, x in enumerate(layers):
-                for n in ("q", "k", "v", "do"):
-                    host_inputs.append(x[n])
-                    dev_inputs.append(dl[i][n])
-            results = [grads[0][0]]
-        elif kind == "chain":
-            layers = make_chain(B, Hq, Hkv, N, D, layers=W["layers"], seed=rank)
-            dl = [{n: x[n].to(dev) for n in ("q", "k", "v")} for x in layers]
-            outs = [(torch.empty_like(x["q"]),
-                     torch.empty((B, Hq, N), dtype=torch.float32, device=dev)) for x in dl]
-            buf = torch.empty((B, Hq, N, N), dtype=torch.float32, device=dev)
-            L = W["layers"]
-            for i in range(L):
-                def layer(i=i):
-                    x, (o, lse) = dl[i], outs[i]
-                    s = ta.raw_attn_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
-                                        buf.data_ptr() if i > 0 else None, o.data_ptr(),
-                                        lse.data_ptr(), B, Hq, Hkv, N, D, scale, causal,
-                                        buf.data_ptr() if i < L - 1 else None, sh)
-                    assert s == 0, s
-                phases.append((f"layer{i}", layer, attn_flops(B, Hq, N, D, causal),
-                               chain_layer_bytes(W, i)))
-            for i, x in enumerate(layers):
-                for n in ("q", "k", "v"):
-                    host_inputs.append(x[n])
-                    dev_inputs.append(dl[i][n])
-            results = [outs[-1][0]]
-        else:
-            x = make_qkv(B, Hq, Hkv, N, D, seed=rank, with_do=(kind == "fwd_bwd"))
-            q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-            o = torch.empty_like(q)
-            lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-
-            window = W.get("window")
-
-            def fwd():
-                if window:
-                    s = ta.raw_attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
-                                               o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
-                                               window, None, sh)
-                else:
-                    s = ta.raw_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), None,
-                                        o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, D, scale,
-                                        causal, None, sh)
-                assert s == 0, s
-            io_bytes = 2 * (B * Hq * N * D) * 2 + 2 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-            phases.append(("fwd", fwd, attn_flops(B, Hq, N, D, causal, window), io_bytes))
-            host_inputs += [x["q"], x["k"], x["v"]]
-            dev_inputs += [q, k, v]
-            results = [o]
-            if kind == "fwd_bwd":
-                do = x["do"].to(dev)
-                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-                ws = torch.empty(max(ta.attn_bwd_workspace_size(B, Hq, Hkv, N, D), 256),
-                                 dtype=torch.uint8, device=dev)
-
-                def bwd():
-                    if window:
-                        s = ta.raw_attn_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                                   o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B,
-                                                   Hq, Hkv, N, D, scale, window, ws.data_ptr(),
-                                                   ws.numel(), sh)
-                    else:
-                        s = ta.raw_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
-                                            dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, D, scale,
-                                            causal, ws.data_ptr(), ws.numel(), sh)
-                    assert s == 0, s
-                bwd_bytes = 4 * (B * Hq * N * D) * 2 + 4 * (B * Hkv * N * D) * 2 + B * Hq * N * 4
-                phases.append(("bwd", bwd, bwd_flops(B, Hq, N, D, causal, window), bwd_bytes))
-                host_inputs.append(x["do"])
-                dev_inputs.append(do)
-                results = [dq, dk, dv]
-        return phases, host_inputs, dev_inputs, results
-
-    phases, host_inputs, dev_inputs, results = build_workload()
-
-    launches = {"fwd": 1, "bwd": 3, "decode": 2}
-    launches.update({f"bwd{i}": 3 for i in range(8)})
-    launches_per_step = sum(launches.get(lbl, 1) for lbl, *_ in phases)
+    phases, host_inputs, dev_inputs, results = build_workload(W, ta, dev, rank, sh)
+    launches_per_step = sum(LAUNCHES.get(lbl, 1) for lbl, *_ in phases)
 
     def step():
         for _, fn, _, _ in phases:
@@ -519,8 +718,6 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     assert ta.attn_last_device_status() == 0
 
-    nph = len(phases)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     try:
         gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
         if not gpu_id.startswith("GPU-"):
@@ -528,35 +725,54 @@ def run_ours(args):
     except Exception:
         gpu_id = str(local)
     sampler = ClockSampler(gpu_id)
+    bytes_step = sum(ph[3] for ph in phases)
+    flops_step = sum(ph[2] for ph in phases)
+    do_flush = wants_flush(args.l2, bytes_step)
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)   # let the sampler start before the load
-    # Between timed steps either flush L2 (write a buffer larger than it) or
-    # rely on a step's own traffic being larger than L2 (more than twice its
-    # size), which leaves nothing of the previous step resident.
-    bytes_per_step = sum(ph[3] for ph in phases)
-    do_flush = args.l2 == "flush" or (args.l2 == "auto" and bytes_per_step <= 2 * L2_BYTES)
-    for i in range(args.steps):
+    # ---- the K timed steps (the line's value)
+    per = time_steps(phases, stream, args.steps, do_flush, flush)
+    barrier(world)
+    status = ta.attn_last_device_status()
+    assert status == 0, ta.attn_status_string(status)
+    step_ms = [sum(p) for p in per]
+    nph = len(phases)
+    ph_avg = [max_over_ranks(sum(p[j] for p in per) / len(per), world, dev) for j in range(nph)]
+    ms_step = max_over_ranks(sum(step_ms) / args.steps, world, dev)
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    # ---- the same step back to back for at least a second, under the same
+    # clock sampling (a steadier figure and enough clock samples)
+    sustained = None
+    if not args.no_sustained:
+        n_sus = max(args.steps, int(math.ceil(args.sustained_s / max(ms_step * 1e-3, 1e-6))))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if do_flush:
-            flush.fill_(float(i))   # untimed: evicts the previous step's data from L2
-        ev[i][0].record(stream)
-        for j, (_, fn, _, _) in enumerate(phases):
-            fn()
-            ev[i][j + 1].record(stream)
+            per_s = time_steps(phases, stream, n_sus, do_flush, flush)
+            sus_ms = sum(sum(p) for p in per_s) / n_sus
+        else:
+            s0.record(stream)
+            for _ in range(n_sus):
+                step()
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            sus_ms = s0.elapsed_time(s1) / n_sus
+        sus_ms = max_over_ranks(sus_ms, world, dev)
+        sustained = {"steps": n_sus, "seconds": n_sus * sus_ms * 1e-3, "ms_per_step": sus_ms,
+                     "value": world * flops_step / (sus_ms * 1e-3) / 1e12}
+        assert ta.attn_last_device_status() == 0
+    # ---- the other configurations (rank 0's GPU, default line only)
+    configs = None
+    if args.workload == "step" and not args.no_configs and rank == 0:
+        configs = {}
+        for cid, wname in CONFIG_SET:
+            configs[cid] = time_config(EXTRA_WORKLOADS[wname], ta, dev, sh, stream, flush,
+                                       args.l2, pk)
+            torch.cuda.empty_cache()
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
-    status = ta.attn_last_device_status()
-    assert status == 0, ta.attn_status_string(status)
-
-    ph_ms = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(nph)]
-    ph_avg = [max_over_ranks(sum(t) / len(t), world, dev) for t in ph_ms]
-    ms_step = max_over_ranks(sum(sum(e[j].elapsed_time(e[j + 1]) for j in range(nph)) for e in ev)
-                             / args.steps, world, dev)
-    flops_step = sum(ph[2] for ph in phases)
-    bytes_step = sum(ph[3] for ph in phases)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
 
     # ------------------------------------------------------------ e2e
     # Every step copies its inputs from pinned host memory to the device and
@@ -571,7 +787,7 @@ def run_ours(args):
         outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
         h2d = sum(t.numel() * t.element_size() for t in pinned)
         d2h = sum(t.numel() * t.element_size() for t in outs_h)
-        phases_b, _, dev_inputs_b, results_b = build_workload()
+        phases_b, _, dev_inputs_b, results_b = build_workload(W, ta, dev, rank, sh)
         sets = [(phases, dev_inputs, results), (phases_b, dev_inputs_b, results_b)]
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         n_e2e = max(4, min(args.steps, 50))
@@ -647,93 +863,37 @@ def run_ours(args):
     # ------------------------------------------------------- roofline
     # The dominant kernel by device time decides the roofline entry; every
     # phase is reported under "kernels".
-    pk = peaks()
-    units = tile_pairs(B, Hq, N, causal, W.get("window"))   # 128x128 tile pairs
-    tag = (f"{'causal' if causal else 'noncausal'}_B{B}_H{Hq}_N{N}_D{D}"
-           + (f"_W{W['window']}" if W.get("window") else ""))
-    kernels = {}
-    for (lbl, _, fl, by), avg in zip(phases, ph_avg):
-        if kind == "decode":
-            ach = by / (avg * 1e-3) / 1e9
-            kernels[lbl] = {"kernel": f"decode_split_kernel<{D}> + decode_merge_kernel",
-                            "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                            "traffic": profiled_traffic(f"decode_split_kernel_{W['name']}",
-                                                        source_digest(DEC_SOURCES),
-                                                        B * Hkv * N),
-                            "bytes_per_launch": by, "flops_per_launch": fl,
-                            "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
-                            "launches_timed": 2,
-                            "source_digest": source_digest(DEC_SOURCES)}
-            continue
-        if kind == "chain_train":
-            is_b = lbl.startswith("bwd")
-            dg = source_digest(BWD_SOURCES if is_b else FWD_SOURCES)
-            ach = by / (avg * 1e-3) / 1e9
-            ctag = f"causal_B{B}_H{Hq}_N{N}_D{D}"
-            kernels[lbl] = {"kernel": ("bwd_main_kernel<%d,causal,residual> (+pre, dQ convert)" % D
-                                       if is_b else f"fwd_kernel<{D},causal,bias/emit>"),
-                            "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-                            "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
-                            "traffic": (profiled_traffic(
-                                f"bwd_main_kernel_residual_chain_train_B{B}_H{Hq}_N{N}_D{D}", dg,
-                                units) if lbl in ("bwd1", "bwd2") else
-                                profiled_traffic(f"fwd_kernel_chain_{ctag}", dg, units)
-                                if lbl in ("fwd1", "fwd2") else None),
-                            "bytes_per_launch": by, "flops_per_launch": fl,
-                            "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
-                            "launches_timed": 3 if is_b else 1, "source_digest": dg}
-            continue
-        if kind == "chain":
-            dg = source_digest(FWD_SOURCES)
-            ach = by / (avg * 1e-3) / 1e9
-            kernels[lbl] = {"kernel": f"fwd_kernel<{D},causal,bias/emit>", "bound": "hbm",
-                            "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                            "frac": ach / pk["hbm_gbs"],
-                            "traffic": profiled_traffic(f"fwd_kernel_chain_{tag}", dg, units),
-                            "bytes_per_launch": by, "flops_per_launch": fl,
-                            "tflops": fl / (avg * 1e-3) / 1e12, "avg_launch_ms": avg,
-                            "launches_timed": 1, "source_digest": dg}
-            continue
-        is_bwd = lbl == "bwd"
-        dg = source_digest(BWD_SOURCES if is_bwd else FWD_SOURCES)
-        ach = fl / (avg * 1e-3) / 1e12
-        name = f"{'bwd_main_kernel' if is_bwd else 'fwd_kernel'}_{tag}"
-        kernels[lbl] = {"kernel": f"{'bwd_main_kernel' if is_bwd else 'fwd_kernel'}<{D},"
-                                  f"{'causal' if causal else 'noncausal'}>",
-                        "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
-                        "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
-                        "traffic": profiled_traffic(name, dg, units),
-                        "flops_per_launch": fl, "units_per_launch": units,
-                        "avg_launch_ms": avg, "launches_timed": 3 if is_bwd else 1,
-                        "source_digest": dg}
-        if is_bwd:
-            kernels[lbl]["timing_note"] = ("CUDA events around attn_bwd: preprocess + main + "
-                                           "dQ convert; the main kernel dominates (ncu launch list)")
+    kernels = kernel_entries(W, phases, ph_avg, pk)
+    for j, (lbl, *_rest) in enumerate(phases):
+        kernels[lbl]["ms"] = pct_stats([p[j] for p in per])
     dom = max(kernels, key=lambda kk: kernels[kk]["avg_launch_ms"])
     roof = dict(kernels[dom])
     roof["peak_source"] = (f"{pk['source']} HBM copy" if roof["bound"] == "hbm"
                            else f"{pk['source']} bf16 burst")
+    if configs is not None and kind == "fwd_bwd":
+        configs["C5"] = {"workload": W["name"], "ms": pct_stats(step_ms), "iters": args.steps,
+                         "tflops": value / world, "frac": value / world / pk["bf16_tflops"],
+                         "peak": pk["bf16_tflops"], "bound": "tensor",
+                         "phases": {lbl: {kk: kernels[lbl][kk] for kk in
+                                          ("kernel", "ms", "achieved", "frac", "traffic",
+                                           "tensor_pipe_active_pct") if kk in kernels[lbl]}
+                                    for lbl in kernels},
+                         "note": "the line's own K timed steps"}
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: q,k,v(,dO) ~ N(0,1) bf16, seeded",
-            "config": dict(config_block(world, W),
-                           step={"fwd_bwd": "forward + backward", "fwd": "forward",
-                                 "decode": "one decode step (stream-K over one block per SM, then merge)",
-                                 "chain_train": "four chained layers forward, then backward "
-                                                "through the block (fp32 residual and gradient)",
-                                 "chain": "four chained forward layers, fp32 residual in place"}[kind],
-                           l2=(f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)"
-                               if do_flush else
-                               f"no flush: inputs larger than L2 (a step moves "
-                               f"{bytes_per_step / 2**20:.0f} MB, over twice the "
-                               f"{L2_BYTES >> 20} MB L2)")),
+            "config": line_config(W, world, do_flush, bytes_step),
+            "ms": pct_stats(step_ms),
             "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
             "hbm_gbs_step": world * bytes_step / (ms_step * 1e-3) / 1e9,
             "roofline": roof, "kernels": kernels, "clocks": clocks,
             "gpu_launches": launches_per_step * args.steps, "e2e": e2e}
+    if sustained is not None:
+        line["sustained"] = sustained
+    if configs is not None:
+        line["configs"] = configs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_min_s, args.cpu_max_s)
     if rank == 0:
@@ -753,6 +913,12 @@ def main():
     ap.add_argument("--workload", default="step", choices=["step", *EXTRA_WORKLOADS],
                     help="step (default): the causal fwd+bwd line; others for manual runs")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (C1-C4) after the default line")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the back-to-back run of the step after the K timed steps")
+    ap.add_argument("--sustained-s", type=float, default=1.0,
+                    help="length of the back-to-back run (seconds)")
     ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
                     help="between timed steps: flush L2, or not (auto: flush unless a step's "
                          "algorithmic bytes exceed twice the L2 size)")

@@ -43,7 +43,10 @@
  *    owned by the caller; bf16 tensors must be 16-byte aligned, fp32 tensors
  *    4-byte aligned.  The library allocates no device memory for its
  *    kernels; the backward takes its scratch from a caller-provided
- *    workspace.  The only device state is one small status word per device.
+ *    workspace.  The only device state is one small status word per device,
+ *    whose address is looked up once per device and cached: the library
+ *    works in each device's primary context and does not support calls
+ *    after cudaDeviceReset (or another teardown of that context).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are asynchronous and stream-ordered: they return after
  *    the launches are queued.
@@ -242,7 +245,10 @@ attn_status attn_bwd_window(const void *q, const void *k, const void *v, const v
  *    attn_bwd with your own workspace for it);
  *  - the first call on a device looks up that device's address of the
  *    scratch array (cudaGetSymbolAddress, with the device current) and
- *    caches it; make that first call before any stream capture;
+ *    caches it; make that first call before any stream capture.  The cached
+ *    address belongs to the device's primary context: calls after
+ *    cudaDeviceReset (or any other teardown of that context) are not
+ *    supported;
  *  - every call shares the one array and the array keeps whatever the last
  *    call left in it; each call first rewrites everything it later reads, so
  *    leftover contents never change a result;
@@ -290,6 +296,30 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int N, int D);
 attn_status attn_decode(const void *q, const void *k, const void *v, void *o, float *lse,
                         int B, int Hq, int Hkv, int N, int D, float scale,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Test hook for the bounded-wait failure path (the pages have no counterpart;
+ * they only advise checking the -inf initialisation when NaNs appear,
+ * "FlashAttention原理与Triton实战" 5.1).
+ *
+ * Runs attn_fwd (no bias, no emitted logits) with a fault injected: thread
+ * block 0's TMA producer never issues its first K tile, so the MMA issuer's
+ * wait for that tile cannot complete.  Every pipeline wait of the launch is
+ * bounded by `wait_limit_ns` nanoseconds instead of the default 1 s.  The
+ * first wait to run out records ATTN_ERR_TIMEOUT in the device status word
+ * and raises the block's abort flag; the block's other roles give up their
+ * waits, let their copies and MMAs in flight land (each with a 20 ms limit of
+ * its own), free their tensor memory and return.  Nothing traps, and the
+ * context stays usable.  The other blocks compute normally; the outputs of
+ * block 0's query tiles are left unwritten.
+ *
+ *   wait_limit_ns  > 0 (ATTN_ERR_INVALID otherwise)
+ * Other arguments, layouts and errors are those of attn_fwd.  Returns ATTN_OK
+ * once queued; attn_last_device_status() then reports ATTN_ERR_TIMEOUT.
+ */
+attn_status attn_debug_fwd_timeout(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int Hq, int Hkv, int N, int D, float scale,
+                                   int causal, unsigned long long wait_limit_ns, void *stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *attn_status_string(attn_status status);

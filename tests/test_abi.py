@@ -170,3 +170,75 @@ def test_bwd_residual_rejects(ta, kw, code):
                                     args["dv"], args["gout"], args["B"], args["Hq"], args["Hkv"],
                                     args["N"], args["D"], args["scale"], args["causal"],
                                     args["ws"], args["ws_bytes"], args["stream"]) == code
+
+
+def noalloc(ta, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, do=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=2, N=256, D=64,
+                scale=0.125, causal=1, stream=None)
+    args.update(kw)
+    return ta.raw_attn_bwd_noalloc(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0, D=0), 1),                      # D is checked before the empty shortcut
+    (dict(B=0, scale=float("nan")), 1),       # and so is the scale
+    (dict(N=0, D=72), 2),
+    (dict(B=0), 0), (dict(Hq=0), 0), (dict(N=0), 0),
+    (dict(B=-1), 1), (dict(Hkv=3), 1), (dict(D=72), 2), (dict(q=None), 1),
+])
+def test_noalloc_codes_match_attn_bwd(ta, kw, code):
+    """attn_bwd_noalloc returns the code attn_bwd would for the same sizes,
+    empty problems included, without launching anything."""
+    assert noalloc(ta, **kw) == code
+    b = dict(kw)
+    for key in ("do", "dq", "dk", "dv"):
+        b.pop(key, None)
+    assert bwd(ta, **b) == code
+
+
+def test_noalloc_scratch_constant_is_the_headers(ta):
+    text = open(os.path.join(ROOT, "include", "tattn.h")).read()
+    m = re.search(r"#define\s+ATTN_BWD_NOALLOC_SCRATCH_BYTES\s+(\d+)", text)
+    assert m and int(m.group(1)) == ta.ATTN_BWD_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_rejects_one_row_past_the_scratch(ta):
+    """The C entry point's own limit sits exactly at the header's size: one
+    head of D = 128 fits up to N = 64526 rows (workspace == scratch) and is
+    refused at N = 64527, before any launch."""
+    S = ta.ATTN_BWD_NOALLOC_SCRATCH_BYTES
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 64526, 128) == S
+    assert ta.attn_bwd_workspace_size(1, 1, 1, 64527, 128) > S
+    assert noalloc(ta, Hq=1, Hkv=1, N=64527, D=128) == ta.ATTN_ERR_UNSUPPORTED
+    assert noalloc(ta, Hq=4, Hkv=2, N=64527, D=128) == ta.ATTN_ERR_UNSUPPORTED
+
+
+def _cpu_bwd_args(B=1, Hq=2, Hkv=1, N=64, D=64):
+    import torch
+    bf = torch.bfloat16
+    q = torch.zeros(B, Hq, N, D, dtype=bf)
+    k = torch.zeros(B, Hkv, N, D, dtype=bf)
+    return dict(q=q, k=k, v=k.clone(), o=q.clone(), lse=torch.zeros(B, Hq, N), do=q.clone())
+
+
+@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_noalloc"])
+@pytest.mark.parametrize("bad", ["dq_shape", "dk_shape", "dv_dtype", "dq_layout", "dk_device"])
+def test_wrappers_reject_bad_output_buffers(ta, fn, bad):
+    """Caller-given dq/dk/dv go through the same checks as the inputs, before
+    any call into the library (CPU tensors here: nothing can launch)."""
+    import torch
+    a = _cpu_bwd_args()
+    q, k = a["q"], a["k"]
+    if bad == "dq_shape":
+        a["dq"], err = torch.zeros(1, 2, 63, 64, dtype=torch.bfloat16), ValueError
+    elif bad == "dk_shape":
+        a["dk"], err = torch.zeros_like(q), ValueError
+    elif bad == "dv_dtype":
+        a["dv"], err = torch.zeros(k.shape), TypeError
+    elif bad == "dq_layout":
+        a["dq"], err = torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16).transpose(2, 3), ValueError
+    else:
+        a["dk"], err = torch.zeros_like(k), TypeError   # right shape, but not on the device
+    kw = {n: a.pop(n) for n in ("dq", "dk", "dv") if n in a}
+    with pytest.raises(err):
+        getattr(ta, fn)(*a.values(), **kw)

@@ -67,3 +67,33 @@ def test_window_counts_reduce_to_causal():
     assert bench.tile_pairs(1, 1, 256, True, 1) == 2
     # W keys per row once i >= W: N*W - W^2/2 pairs in the continuous count
     assert bench.attn_flops(1, 1, 1000, 1, True, 100) == 4.0 * (1000 * 100 - 100 * 100 / 2)
+
+
+def test_median_p90_min(bench):
+    """The pages' bench template reports median, p90 and min of the timed
+    iterations; p90 by nearest rank."""
+    st = bench.pct_stats([float(x) for x in range(10, 0, -1)])
+    assert st == {"median": 5.5, "p90": 9.0, "min": 1.0}
+    assert bench.pct_stats([2.0]) == {"median": 2.0, "p90": 2.0, "min": 2.0}
+
+
+def test_profile_summary_is_read_only_at_its_own_digest(bench, tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "k_x.md").write_text(
+        "source_digest: abc123\ndram_bytes_per_launch: 1000\nunits_per_launch: 10\n"
+        "tensor_pipe_active_pct: 61.5\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench.profiled("k_x", "abc123", 40)
+    assert p["traffic"] == 4000 and p["tensor_pipe_active_pct"] == 61.5
+    assert "scaled" in p["traffic_basis"]
+    assert bench.profiled("k_x", "abc123", 10)["traffic_basis"] == "measured at this size"
+    assert bench.profiled("k_x", "ffffff", 10) == {}     # kernel changed since the capture
+    assert bench.profiled("missing", "abc123", 10) == {}
+
+
+def test_both_arms_print_the_same_config(bench):
+    W = bench.WORKLOAD
+    a = bench.line_config(W, 1, bench.wants_flush("auto", bench.workload_bytes(W)),
+                          bench.workload_bytes(W))
+    assert a["workload"] == W["name"] and a["step"] == "forward + backward"
+    assert a["l2"].startswith("no flush")

@@ -218,3 +218,25 @@ def test_chain_full_size_sampled(ta, orc):
         if i < 3:
             check_logits(snaps[i], ref["logits"], f"logits {i}")
         prev = np.ascontiguousarray(ref["logits"])
+
+
+def test_chain_full_size_every_element(ta, orc):
+    """The 4-layer block at full size (B=1, 20 query heads, 4 kv heads,
+    N=4096, D=128, causal), every output element and every kept emitted logit
+    against the oracle's own chain (fp64 logits carried layer to layer)."""
+    B, Hq, Hkv, N, D = 1, 20, 4, 4096, 128
+    layers = make_chain(B, Hq, Hkv, N, D, layers=4, seed=0)
+    outs, snaps = run_chain_gpu(ta, layers, causal=True)
+    prev = None
+    for i, x in enumerate(layers):
+        ref = orc.forward(*orc_in(x), scale=1 / math.sqrt(D), causal=True,
+                          bias=prev, emit_logits=True)
+        check_o(outs[i][0], ref["o"], f"layer {i}")
+        check_lse(outs[i][1], ref["lse"], f"layer {i}")
+        if i < 3:
+            check_logits(snaps[i], ref["logits"], f"logits {i}")
+            snaps[i] = None
+            # The next layer's bias: the kept logits (masked entries never
+            # reach a result; zero them so the oracle reads finite numbers).
+            prev = np.nan_to_num(ref["logits"], nan=0.0, copy=False)
+        del ref

@@ -224,3 +224,24 @@ def test_causal_head_chunked_order(ta, orc):
     r = torch.from_numpy(rows).cuda()
     check_o(o.reshape(-1, D)[r], ref["o"], "head-chunked causal")
     check_lse(lse.reshape(-1)[r], ref["lse"], "head-chunked causal")
+
+
+# Every element of the two forward configurations against the oracle, as
+# the pages' own checks compare whole outputs (max-abs and mean-abs:
+# blog.ans20xx.com day26, "数值对齐检查"; kwkr.cn/news/592482, 3.4).  The
+# oracle takes about 70 GFLOP (C3) and 550 GFLOP (C2) of fp64 work.
+FULL_EVERY_ELEMENT = [
+    ("C2_noncausal_8x32x2048x128", 8, 32, 32, 2048, 128, False),
+    ("C3_causal_2x16x4096x64", 2, 16, 16, 4096, 64, True),
+]
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,N,D,causal", FULL_EVERY_ELEMENT,
+                         ids=[f[0] for f in FULL_EVERY_ELEMENT])
+def test_parity_full_size_every_element(ta, orc, name, B, Hq, Hkv, N, D, causal):
+    x = make_qkv(B, Hq, Hkv, N, D, seed=0)
+    o, lse = run_fwd(ta, x, causal=causal)
+    ref = oracle_fwd(orc, x, causal, 1 / math.sqrt(D))
+    mx, mean = check_o(o, ref["o"], name)
+    lmx = check_lse(lse, ref["lse"], name)
+    print(f"{name}: O max-abs {mx:.3e} mean-abs {mean:.3e}, LSE max-abs {lmx:.3e}")

@@ -44,10 +44,23 @@ ATTN_ERR_DEVICE_CHECK = 5
 EXPORTED = ("attn_fwd", "attn_fwd_window", "attn_bwd_workspace_size", "attn_bwd",
             "attn_bwd_window", "attn_bwd_residual", "attn_bwd_noalloc", "attn_decode_workspace_size", "attn_decode",
             "attn_status_string",
-            "attn_last_device_status", "attn_version")
+            "attn_last_device_status", "attn_version", "attn_debug_fwd_timeout")
 
-# Size of the fixed device scratch attn_bwd_noalloc uses (include/tattn.h).
-ATTN_BWD_NOALLOC_SCRATCH_BYTES = 33554432
+
+def _header_define(name: str) -> int:
+    """An integer #define of include/tattn.h, read from the header the library
+    is compiled against (one source for the value, no copy of it here)."""
+    import re
+    path = os.path.join(os.path.dirname(_HERE), "include", "tattn.h")
+    with open(path) as f:
+        m = re.search(r"^#define\s+" + name + r"\s+(\d+)\s*$", f.read(), flags=re.M)
+    if not m:
+        raise RuntimeError(f"{name} not found in {path}")
+    return int(m.group(1))
+
+
+# Size of the fixed device scratch attn_bwd_noalloc uses.
+ATTN_BWD_NOALLOC_SCRATCH_BYTES = _header_define("ATTN_BWD_NOALLOC_SCRATCH_BYTES")
 
 _lock = threading.Lock()
 _lib = None
@@ -97,6 +110,9 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_workspace_size.restype = sz
             L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
             L.attn_decode.restype = i
+            L.attn_debug_fwd_timeout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i,
+                                                 ctypes.c_ulonglong, vp]
+            L.attn_debug_fwd_timeout.restype = i
             L.attn_status_string.argtypes = [i]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_last_device_status.argtypes = [vp]
@@ -125,17 +141,31 @@ def _ptr(t) -> int | None:
 
 
 def _check(t, name, dtype, shape):
+    """Type, shape and layout of one tensor argument (None passes)."""
     import torch
     if t is None:
         return
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _check_all(specs, device):
+    """Checks every (tensor, name, dtype, shape) of a call, inputs and
+    caller-given outputs alike, before anything reaches the library: first
+    type, shape and layout, then that each lives on `device` (a CUDA
+    device).  A wrong output buffer would otherwise be written out of
+    bounds by the kernels."""
+    for t, name, dt, shp in specs:
+        _check(t, name, dt, shp)
+    for t, name, _, _ in specs:
+        if t is not None and (not t.is_cuda or t.device != device):
+            raise TypeError(f"{name} must be a CUDA tensor on {device}, got {t.device}")
 
 
 def raw_attn_fwd(q, k, v, bias, o, lse, B, Hq, Hkv, N, D, scale, causal, emit, stream) -> int:
@@ -185,17 +215,17 @@ def attn_fwd(q, k, v, bias=None, *, scale: float | None = None, causal: bool = F
     Hkv = k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    _check(q, "q", torch.bfloat16, (B, Hq, N, D))
-    _check(k, "k", torch.bfloat16, (B, Hkv, N, D))
-    _check(v, "v", torch.bfloat16, (B, Hkv, N, D))
-    _check(bias, "bias", torch.float32, (B, Hq, N, N))
-    _check(emit_logits, "emit_logits", torch.float32, (B, Hq, N, N))
+    _check_all(((q, "q", torch.bfloat16, (B, Hq, N, D)),
+                (k, "k", torch.bfloat16, (B, Hkv, N, D)),
+                (v, "v", torch.bfloat16, (B, Hkv, N, D)),
+                (bias, "bias", torch.float32, (B, Hq, N, N)),
+                (emit_logits, "emit_logits", torch.float32, (B, Hq, N, N)),
+                (o, "o", torch.bfloat16, (B, Hq, N, D)),
+                (lse, "lse", torch.float32, (B, Hq, N))), q.device)
     if o is None:
         o = torch.empty_like(q)
-    _check(o, "o", torch.bfloat16, (B, Hq, N, D))
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    _check(lse, "lse", torch.float32, (B, Hq, N))
     if window is not None:
         if not causal:
             raise ValueError("a sliding window needs causal=True")
@@ -208,6 +238,24 @@ def attn_fwd(q, k, v, bias=None, *, scale: float | None = None, causal: bool = F
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
     return o, lse
+
+
+def _bwd_specs(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D):
+    import torch
+    bf = torch.bfloat16
+    return ((q, "q", bf, (B, Hq, N, D)), (k, "k", bf, (B, Hkv, N, D)),
+            (v, "v", bf, (B, Hkv, N, D)), (o, "o", bf, (B, Hq, N, D)),
+            (lse, "lse", torch.float32, (B, Hq, N)), (do, "do", bf, (B, Hq, N, D)),
+            (dq, "dq", bf, (B, Hq, N, D)), (dk, "dk", bf, (B, Hkv, N, D)),
+            (dv, "dv", bf, (B, Hkv, N, D)))
+
+
+def raw_attn_debug_fwd_timeout(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, causal, wait_limit_ns,
+                               stream) -> int:
+    """Test hook: the forward with block 0's first K load left out and every
+    pipeline wait bounded by `wait_limit_ns` (see include/tattn.h)."""
+    return lib().attn_debug_fwd_timeout(q, k, v, o, lse, B, Hq, Hkv, N, D, ctypes.c_float(scale),
+                                        int(causal), int(wait_limit_ns), stream)
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, D: int) -> int:
@@ -228,13 +276,18 @@ def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = 
     Hkv = k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    for t, name, dt, shp in ((q, "q", torch.bfloat16, (B, Hq, N, D)),
-                             (k, "k", torch.bfloat16, (B, Hkv, N, D)),
-                             (v, "v", torch.bfloat16, (B, Hkv, N, D)),
-                             (o, "o", torch.bfloat16, (B, Hq, N, D)),
-                             (lse, "lse", torch.float32, (B, Hq, N)),
-                             (do, "do", torch.bfloat16, (B, Hq, N, D))):
-        _check(t, name, dt, shp)
+    residual = bias is not None or grad_in is not None or grad_out is not None
+    if residual and window is not None:
+        raise ValueError("the residual backward takes no window")
+    if workspace is not None and (not isinstance(workspace, torch.Tensor)
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous tensor")
+    _check_all(_bwd_specs(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D)
+               + ((bias, "bias", torch.float32, (B, Hq, N, N)),
+                  (grad_in, "grad_in", torch.float32, (B, Hq, N, N)),
+                  (grad_out, "grad_out", torch.float32, (B, Hq, N, N)),
+                  (workspace, "workspace", None if workspace is None else workspace.dtype,
+                   None if workspace is None else tuple(workspace.shape))), q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -242,11 +295,7 @@ def attn_bwd(q, k, v, o, lse, do, *, scale: float | None = None, causal: bool = 
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    if bias is not None or grad_in is not None or grad_out is not None:
-        if window is not None:
-            raise ValueError("the residual backward takes no window")
-        for t, name in ((bias, "bias"), (grad_in, "grad_in"), (grad_out, "grad_out")):
-            _check(t, name, torch.float32, (B, Hq, N, N))
+    if residual:
         st = raw_attn_bwd_residual(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                    _ptr(bias), _ptr(grad_in), _ptr(dq), _ptr(dk), _ptr(dv),
                                    _ptr(grad_out), B, Hq, Hkv, N, D, scale, causal,
@@ -283,13 +332,7 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, *, scale: float | None = None, causal:
     Hkv = k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    for t, name, dt, shp in ((q, "q", torch.bfloat16, (B, Hq, N, D)),
-                             (k, "k", torch.bfloat16, (B, Hkv, N, D)),
-                             (v, "v", torch.bfloat16, (B, Hkv, N, D)),
-                             (o, "o", torch.bfloat16, (B, Hq, N, D)),
-                             (lse, "lse", torch.float32, (B, Hq, N)),
-                             (do, "do", torch.bfloat16, (B, Hq, N, D))):
-        _check(t, name, dt, shp)
+    _check_all(_bwd_specs(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, N, D), q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -319,14 +362,19 @@ def attn_decode(q, k, v, *, scale: float | None = None, o=None, lse=None, want_l
     Hkv, N = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    _check(q, "q", torch.bfloat16, (B, Hq, D))
-    _check(k, "k", torch.bfloat16, (B, Hkv, N, D))
-    _check(v, "v", torch.bfloat16, (B, Hkv, N, D))
+    if workspace is not None and (not isinstance(workspace, torch.Tensor)
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous tensor")
+    _check_all(((q, "q", torch.bfloat16, (B, Hq, D)),
+                (k, "k", torch.bfloat16, (B, Hkv, N, D)),
+                (v, "v", torch.bfloat16, (B, Hkv, N, D)),
+                (o, "o", torch.bfloat16, (B, Hq, D)),
+                (lse, "lse", torch.float32, (B, Hq)),
+                (workspace, "workspace", None if workspace is None else workspace.dtype,
+                 None if workspace is None else tuple(workspace.shape))), q.device)
     o = torch.empty_like(q) if o is None else o
-    _check(o, "o", torch.bfloat16, (B, Hq, D))
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    _check(lse, "lse", torch.float32, (B, Hq))
     if workspace is None:
         need = attn_decode_workspace_size(B, Hq, Hkv, N, D)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

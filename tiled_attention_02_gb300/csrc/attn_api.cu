@@ -145,7 +145,8 @@ namespace {
 // window: 0 for none, else W >= 1 (checked by the caller; implies causal).
 attn_status fwd_impl(const void *q, const void *k, const void *v, const float *bias, void *o,
                      float *lse, int B, int Hq, int Hkv, int N, int D, float scale, int causal,
-                     int window, float *emit_logits, void *stream) {
+                     int window, float *emit_logits, void *stream,
+                     unsigned long long wait_limit_ns = 0, int inject_skip_k0 = 0) {
     bool empty = false;
     attn_status st = check_sizes(B, Hq, Hkv, N, D, scale, &empty);
     if (st != ATTN_OK || empty) return st;
@@ -176,6 +177,8 @@ attn_status fwd_impl(const void *q, const void *k, const void *v, const float *b
     pb.scale = scale;
     pb.causal = causal != 0;
     pb.window = (window > 0 && window < N) ? window : 0;   // W >= N is the causal mask
+    pb.wait_limit_ns = wait_limit_ns;
+    pb.inject_skip_k0 = inject_skip_k0;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
     cudaError_t e = launch_fwd(pb, status, static_cast<cudaStream_t>(stream));
@@ -364,6 +367,14 @@ attn_status attn_bwd_window(const void *q, const void *k, const void *v, const v
     if (window < 1) return ATTN_ERR_INVALID;
     return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, D, scale, 1, window,
                     workspace, workspace_bytes, stream);
+}
+
+attn_status attn_debug_fwd_timeout(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int Hq, int Hkv, int N, int D, float scale,
+                                   int causal, unsigned long long wait_limit_ns, void *stream) {
+    if (wait_limit_ns == 0) return ATTN_ERR_INVALID;
+    return fwd_impl(q, k, v, nullptr, o, lse, B, Hq, Hkv, N, D, scale, causal, 0, nullptr,
+                    stream, wait_limit_ns, 1);
 }
 
 const char *attn_status_string(attn_status s) {

@@ -282,7 +282,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
-    const AbortCtl ac{abort_flag, p.status};
+    const AbortCtl ac{abort_flag, p.status, kWaitLimitNs};
     auto item_qi = [&](int j) { return q_lo + j % nq; };
     auto item_bhq = [&](int j) { return b * p.Hq + g * p.group + hs * hper + j / nq; };
     const uint32_t s_rows = sb + C::kOffRows;   // lse2[s][128] then delta[s][128]

@@ -187,7 +187,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
-    const AbortCtl ac{abort_flag, p.status};
+    const AbortCtl ac{abort_flag, p.status, kWaitLimitNs};
     float *sScore = reinterpret_cast<float *>(smem + C::kOffScore);   // [16 heads][128 keys]
     float *sAlpha = reinterpret_cast<float *>(smem + C::kOffAlpha);   // [16]
 

@@ -152,6 +152,11 @@ struct FwdParams {
     float scale_log2;   // scale * log2(e)
     int window;         // causal sliding window W (key j kept iff i - W < j), 0 = none
     int hchunk;         // causal item order: heads per chunk (BH: a single chunk)
+    unsigned long long wait_limit_ns;   // bound of every pipeline wait
+    // Fault injection for tests of the timeout path: nonzero makes block 0's
+    // producer skip its first K load, so the MMA issuer's wait for it runs
+    // out.  0 in every ordinary launch.
+    int inject_skip_k0;
 };
 
 // O *= alpha on NC consecutive TMEM columns of this thread's row.
@@ -276,7 +281,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
-    const AbortCtl ac{abort_flag, p.status};
+    const AbortCtl ac{abort_flag, p.status, p.wait_limit_ns};
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -371,11 +376,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (t >= C::kKStages &&
                     !mbar_wait(bar(C::kBarKEmpty + ks), ((t / C::kKStages) - 1) & 1, ac))
                     return false;
-                mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &tmK,
-                                bar(C::kBarKFull + ks), c * 64, (ki.kv_lo + kj) * kBlockN,
-                                ki.bh_kv);
+                // (Injected fault: block 0 never loads its first K tile; the
+                // tile still counts as issued, so the abort path's drain waits
+                // for it, with its own short limit.)
+                if (!(p.inject_skip_k0 && blockIdx.x == 0 && t == 0)) {
+                    mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
+                                    &tmK, bar(C::kBarKFull + ks), c * 64,
+                                    (ki.kv_lo + kj) * kBlockN, ki.bh_kv);
+                }
                 k_issued = t + 1;
                 advance(kr, kj, ki, k_done);
                 return true;
@@ -904,6 +914,8 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     prm.scale = pb.scale;
     prm.scale_log2 = pb.scale * kLog2e;
     prm.window = pb.causal ? pb.window : 0;
+    prm.wait_limit_ns = pb.wait_limit_ns ? pb.wait_limit_ns : kWaitLimitNs;
+    prm.inject_skip_k0 = pb.inject_skip_k0;
     const long long n_items = static_cast<long long>(prm.n_qtiles) * BH;
     // Causal item order: one chunk of all heads unless their K/V is over
     // twice the L2; then chunks whose K/V is about half the L2, so that the

@@ -20,6 +20,10 @@ struct FwdProblem {
     float scale;
     bool causal;
     int window;      // sliding window W (causal only): key j kept iff i - W < j; 0 = none
+    // Tests of the timeout path only (0 otherwise): the bound of each
+    // pipeline wait (0 = the default) and the injected missing K load.
+    unsigned long long wait_limit_ns = 0;
+    int inject_skip_k0 = 0;
 };
 
 // Validated backward problem.

@@ -48,15 +48,21 @@ extern "C" attn_status attn_bwd_noalloc(const void *q, const void *k, const void
                                         const void *o, const float *lse, const void *dO, void *dq,
                                         void *dk, void *dv, int B, int Hq, int Hkv, int N, int D,
                                         float scale, int causal, void *stream) {
-    if (B < 0 || Hq < 0 || Hkv < 0 || N < 0) return ATTN_ERR_INVALID;
-    if (B == 0 || Hq == 0 || N == 0) return ATTN_OK;   // empty problem: nothing to do
     const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, N, D);
     if (need == 0) {
-        // Invalid or unsupported sizes: let attn_bwd's own checks name which.
+        // An empty problem, or invalid or unsupported sizes: attn_bwd's own
+        // checks (D and scale included) give the same code it would give,
+        // before it touches the missing workspace.
         return attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, D, scale, causal,
                         nullptr, 0, stream);
     }
     if (need > static_cast<size_t>(ATTN_BWD_NOALLOC_SCRATCH_BYTES)) return ATTN_ERR_UNSUPPORTED;
+    // Pointer checks come before the scratch lookup (a CUDA call), so that a
+    // bad argument gives attn_bwd's code without touching the device.
+    const void *bf[] = {q, k, v, o, dO, dq, dk, dv};
+    for (const void *p : bf)
+        if (!p || reinterpret_cast<uintptr_t>(p) % 16 != 0) return ATTN_ERR_INVALID;
+    if (!lse || reinterpret_cast<uintptr_t>(lse) % 4 != 0) return ATTN_ERR_INVALID;
     void *scratch = tattn::scratch_ptr();
     if (!scratch) return ATTN_ERR_CUDA;
     // The backward's first kernel rewrites every scratch byte the later ones

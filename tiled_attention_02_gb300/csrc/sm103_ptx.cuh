@@ -17,8 +17,9 @@ namespace tattn {
 // Device status codes, the same values as attn_status in tattn.h.
 enum : int { kStatusOk = 0, kStatusTimeout = 4, kStatusDeviceCheck = 5 };
 
-// A pipeline wait gives up after this long (ns of %globaltimer).  Every wait
-// in these kernels normally completes within microseconds.
+// A pipeline wait gives up after this long (ns of %globaltimer) unless the
+// launch sets another limit.  Every wait in these kernels normally completes
+// within microseconds.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -106,8 +107,9 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
 // status word and raises the CTA-wide abort flag; every other wait sees the
 // flag and gives up too, so all roles reach the common exit.
 struct AbortCtl {
-    volatile int *flag;   // shared memory
-    int *status;          // global status word
+    volatile int *flag;              // shared memory
+    int *status;                     // global status word
+    unsigned long long limit_ns;     // how long one wait may take
 };
 
 // Bounded wait by one thread.  Returns false on timeout or abort.
@@ -118,7 +120,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*ac.flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > ac.limit_ns) {
                 *ac.flag = 1;
                 atomicCAS(ac.status, kStatusOk, kStatusTimeout);
                 return false;
