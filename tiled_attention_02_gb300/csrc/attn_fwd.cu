@@ -892,6 +892,8 @@ cudaError_t launch_d(bool causal, int ext, const FwdMaps &m, const FwdParams &pr
 }  // namespace
 
 cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
+    // The plain forward runs two query tiles per thread block (attn_fwd_pp.cu).
+    if (!pb.bias && !pb.emit) return launch_fwd_pp(pb, status, stream);
     const long long BH = static_cast<long long>(pb.B) * pb.Hq;
     const long long BHkv = static_cast<long long>(pb.B) * pb.Hkv;
     FwdMaps m;

@@ -88,6 +88,9 @@ bool encode_f32_rows(CUtensorMap *map, const void *base, int D, int N, long long
 int *device_status_ptr();
 
 cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream);
+// The plain forward (no bias, no emitted logits) with two query tiles per
+// thread block (attn_fwd_pp.cu).
+cudaError_t launch_fwd_pp(const FwdProblem &pb, int *status, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdProblem &pb, int *status, cudaStream_t stream);
 cudaError_t launch_decode(const DecProblem &pb, int *status, cudaStream_t stream);
 
