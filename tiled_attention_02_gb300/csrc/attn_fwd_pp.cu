@@ -77,7 +77,7 @@ struct PPCfg {
     static constexpr int kChunkBytes = kBlockM * 128;
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kKStages = D == 64 ? 4 : 2;
-    static constexpr int kVStages = kKStages;
+    static constexpr int kVStages = kKStages;   // (merged K / V stages need equal counts)
     static constexpr int kOffQ = 0;                          // Q_A, Q_B
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
@@ -108,6 +108,10 @@ struct PPCfg {
     static constexpr uint32_t kColO = kSepP ? 384 : 256;
     static constexpr uint32_t kOStride = kSepP ? 64 : 128;
     static constexpr int kIssuers = kSepP ? 2 : 1;   // MMA-issuing threads
+    // With separate P, K_j and V_j of a stage load together, under one
+    // barrier (the K stage's), and the stage is released after its PVs: one
+    // wait per key tile fewer for each issuer.
+    static constexpr bool kMergeKV = kSepP;
     static_assert(kUsed <= kSmemBudget, "shared memory budget");
 };
 
@@ -358,13 +362,25 @@ fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     // it still counts as issued, and the drain below waits
                     // for it with its own short limit.)
                     if (!(p.inject_skip_k0 && blockIdx.x == 0 && t == 0)) {
-                        mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
+                        mbar_arrive_expect_tx(bar(C::kBarKFull + ks),
+                                              C::kMergeKV ? 2 * C::kTileBytes : C::kTileBytes);
                         for (int c = 0; c < C::kChunks; ++c)
                             tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
                                         &tmK, bar(C::kBarKFull + ks), c * 64, j * kBlockN,
                                         itm.bh_kv);
                     }
                     const int vs = t % C::kVStages;
+                    if (C::kMergeKV) {
+                        // V_t on K_t's barrier (armed above for both tiles;
+                        // the injected fault leaves out both).
+                        if (!(p.inject_skip_k0 && blockIdx.x == 0 && t == 0))
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_3d(sb + C::kOffV + vs * C::kTileBytes +
+                                                c * C::kChunkBytes,
+                                            &tmV, bar(C::kBarKFull + ks), c * 64, j * kBlockN,
+                                            itm.bh_kv);
+                        continue;
+                    }
                     if (t >= C::kVStages &&
                         !(ok = mbar_wait(bar(C::kBarVEmpty + vs), ((t / C::kVStages) - 1) & 1, ac))) {
                         ++t;   // K_t was issued
@@ -385,8 +401,9 @@ fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (nq[T] > 0) drain_wait(bar(C::kBarQFull + T), (nq[T] - 1) & 1);
                 for (int u = max(t - C::kKStages, 0); u < t; ++u)
                     drain_wait(bar(C::kBarKFull + u % C::kKStages), (u / C::kKStages) & 1);
-                for (int u = max(t - C::kVStages, 0); u < t; ++u)
-                    drain_wait(bar(C::kBarVFull + u % C::kVStages), (u / C::kVStages) & 1);
+                if (!C::kMergeKV)
+                    for (int u = max(t - C::kVStages, 0); u < t; ++u)
+                        drain_wait(bar(C::kBarVFull + u % C::kVStages), (u / C::kVStages) & 1);
             }
         }
         __syncwarp();
@@ -483,13 +500,15 @@ fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (st.j == st.itm.hi(T)) mma_commit(bar(C::kBarQEmpty + T));
                     ++sc;
                 }
-                mma_commit(bar(C::kBarKEmpty + ks));
+                if (!C::kMergeKV) mma_commit(bar(C::kBarKEmpty + ks));
                 return true;
             };
             auto issue_pv_step = [&](const Step &st, int t) -> bool {
                 const bool in = in_tile(st);
                 const int vs = t % C::kVStages;
-                if (!mbar_wait(bar(C::kBarVFull + vs), (t / C::kVStages) & 1, ac)) return false;
+                if (!C::kMergeKV &&
+                    !mbar_wait(bar(C::kBarVFull + vs), (t / C::kVStages) & 1, ac))
+                    return false;
                 if (in) {
                     if (!mbar_wait(bar(C::kBarPFull + T), pc & 1, ac)) return false;
                     tc_fence_after();
@@ -498,7 +517,9 @@ fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (st.j == st.itm.hi(T)) mma_commit(bar(C::kBarOFinal + T));
                     ++pc;
                 }
-                mma_commit(bar(C::kBarVEmpty + vs));
+                // (Merged stages: K_t and V_t go back together, after the PV;
+                // this issuer waited for the stage in its S step.)
+                mma_commit(bar(C::kMergeKV ? C::kBarKEmpty + vs : C::kBarVEmpty + vs));
                 return true;
             };
             bool ok = true;
@@ -671,29 +692,23 @@ fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const uint64_t cm2 = f2pack(xmul, xmul);
                 const uint64_t nm2 = f2pack(-m_use, -m_use);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                // P as packed bf16 pairs: keys 2c, 2c+1 of the tile in column c.
+                uint32_t pk[kBlockN / 2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // P as packed bf16 pairs: keys 2c, 2c+1 of the tile in
-                    // column c (half h: columns 32h .. 32h + 31).
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int e = 64 * h + 2 * c;
-                        float t0, t1;
-                        f2unpack(ffma2(f2pack(x[e], x[e + 1]), cm2, nm2), t0, t1);
-                        const float p0 = ex2(t0), p1 = ex2(t1);
-                        acc[c & 3] = fadd2(acc[c & 3], f2pack(p0, p1));
-                        pk[c] = pack_bf16x2(p0, p1);
-                    }
-                    if (C::kSepP && h == 0 && t > 0) {
-                        // PV_T(j-1) must be done with the P buffer (and with
-                        // O, which may be rescaled below).
-                        if (!(ok = mbar_wait_warp(bar(C::kBarPVDone + T), (t - 1) & 1, ac))) break;
-                        tc_fence_after();
-                    }
-                    tmem_st32(tP + 32 * h, pk);
+                for (int c = 0; c < kBlockN / 2; ++c) {
+                    float t0, t1;
+                    f2unpack(ffma2(f2pack(x[2 * c], x[2 * c + 1]), cm2, nm2), t0, t1);
+                    const float p0 = ex2(t0), p1 = ex2(t1);
+                    acc[c & 3] = fadd2(acc[c & 3], f2pack(p0, p1));
+                    pk[c] = pack_bf16x2(p0, p1);
                 }
-                if (!ok) break;
+                if (C::kSepP && t > 0) {
+                    // PV_T(j-1) must be done with the P buffer (and with O,
+                    // which may be rescaled below).
+                    if (!(ok = mbar_wait_warp(bar(C::kBarPVDone + T), (t - 1) & 1, ac))) break;
+                    tc_fence_after();
+                }
+                tmem_st64(tP, pk);
                 float sum;
                 {
                     const uint64_t a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
