@@ -87,8 +87,12 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-FWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_fwd.cu",
+# The plain forward kernel (two query tiles per block) and the residual
+# forward (bias / emitted logits) live in separate files.
+FWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_fwd_pp.cu",
                "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
+RES_FWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_fwd.cu",
+                   "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
 BWD_SOURCES = ["tiled_attention_02_gb300/csrc/attn_bwd.cu",
                "tiled_attention_02_gb300/csrc/sm103_ptx.cuh"]
 DEC_SOURCES = ["tiled_attention_02_gb300/csrc/attn_decode.cu",
@@ -594,7 +598,7 @@ def kernel_entries(W, phases, ph_ms, pk):
             continue
         if kind in ("chain", "chain_train"):
             is_b = lbl.startswith("bwd")
-            dg = source_digest(BWD_SOURCES if is_b else FWD_SOURCES)
+            dg = source_digest(BWD_SOURCES if is_b else RES_FWD_SOURCES)
             ach = by / (avg * 1e-3) / 1e9
             if is_b:
                 prof = profiled(f"bwd_main_kernel_residual_chain_train_B{B}_H{Hq}_N{N}_D{D}", dg,
@@ -614,7 +618,7 @@ def kernel_entries(W, phases, ph_ms, pk):
         is_bwd = lbl == "bwd"
         dg = source_digest(BWD_SOURCES if is_bwd else FWD_SOURCES)
         ach = fl / (avg * 1e-3) / 1e12
-        kname = "bwd_main_kernel" if is_bwd else "fwd_kernel"
+        kname = "bwd_main_kernel" if is_bwd else "fwd_pp_kernel"
         kernels[lbl] = dict({"kernel": f"{kname}<{D},{'causal' if causal else 'noncausal'}>",
                              "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                              "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"]},

@@ -1,4 +1,6 @@
-// attn_fwd.cu -- tiled exact-attention forward for GB300 (sm_103a).
+// attn_fwd.cu -- tiled exact-attention forward with a logit bias and / or
+// emitted logits (the block attention residual), for GB300 (sm_103a).  The
+// plain forward, without either, is attn_fwd_pp.cu.
 //
 // One CTA computes one 128-row query tile of one (batch, query head):
 //
@@ -37,8 +39,7 @@
 //
 // The residual variants (bias and/or emitted logits) move 2 x 64 KB of fp32
 // per 128 x 128 tile, several times the tile's MMA time at HBM bandwidth, so
-// their data path is what bounds them.  Three variants (template EXT):
-//   0  no bias, no emit;
+// their data path is what bounds them.  Two variants (template EXT):
 //   2  staged: the bias tile is cut into four 128 x 32 fp32 chunks (one
 //      128-byte swizzle atom wide) that warp 10 TMA-loads into a ring of
 //      shared-memory slots; each softmax thread reads its row of a chunk,
@@ -75,16 +76,13 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpLoader = 10;       // staged residual only
 constexpr int kWarpStorer = 11;       // staged residual only
-constexpr int kWarpOStore = 10;       // persistent plain forward: output tile storer
 
-// The plain forward (no residual) runs persistent blocks, one per SM, each
-// walking a list of (query tile, head) items; the residual variants take one
-// item per block.
+// (The plain forward, without bias or emitted logits, is attn_fwd_pp.cu.)
 template <int EXT>
-constexpr bool fwd_persistent() { return EXT == 0; }
-
-template <int EXT>
-constexpr int fwd_threads() { return EXT == 2 ? 384 : (EXT == 0 ? 352 : 320); }
+constexpr int fwd_threads() {
+    static_assert(EXT == 1 || EXT == 2, "residual variants only");
+    return EXT == 2 ? 384 : 320;
+}
 
 template <int D, int EXT>
 struct FwdCfg {
@@ -102,9 +100,7 @@ struct FwdCfg {
     // needed a whole softmax after its load is issued, so one V stage holds).
     static constexpr int kKStages = (D == 64) ? (EXT == 2 ? 2 : 3) : (EXT == 2 ? 1 : 2);
     static constexpr int kVStages = kKStages;
-    // Two Q buffers in the persistent variant: the next item's Q loads while
-    // this item's output is staged in (and stored from) its own Q buffer.
-    static constexpr int kQBufs = fwd_persistent<EXT>() ? 2 : 1;
+    static constexpr int kQBufs = 1;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBufs * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
@@ -115,10 +111,8 @@ struct FwdCfg {
     static constexpr int kResRing = kResSlots > 0 ? kResSlots : 1;
     static constexpr int kOffBar = kOffRes + kResSlots * kResChunkBytes;
     // barrier indices
-    static constexpr int kBarQFull = 0;                       // 2 (per Q buffer)
-    static constexpr int kBarQEmpty = 2;                      // 2
-    static constexpr int kBarOStaged = 4;                     // 2: output tile staged in that Q buffer
-    static constexpr int kBarKFull = 6;
+    static constexpr int kBarQFull = 0;                       // the Q tile
+    static constexpr int kBarKFull = 1;
     static constexpr int kBarKEmpty = kBarKFull + kKStages;
     static constexpr int kBarVFull = kBarKEmpty + kKStages;
     static constexpr int kBarVEmpty = kBarVFull + kVStages;
@@ -153,10 +147,6 @@ struct FwdParams {
     int window;         // causal sliding window W (key j kept iff i - W < j), 0 = none
     int hchunk;         // causal item order: heads per chunk (BH: a single chunk)
     unsigned long long wait_limit_ns;   // bound of every pipeline wait
-    // Fault injection for tests of the timeout path: nonzero makes block 0's
-    // producer skip its first K load, so the MMA issuer's wait for it runs
-    // out.  0 in every ordinary launch.
-    int inject_skip_k0;
 };
 
 // O *= alpha on NC consecutive TMEM columns of this thread's row.
@@ -285,13 +275,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(C::kBarQFull + s), 1);
-            mbar_init(bar(C::kBarQEmpty + s), 1);   // the output storer
-            // One per buffer: an item's output can only be staged once the
-            // item two back has been stored, so the phases cannot run ahead.
-            mbar_init(bar(C::kBarOStaged + s), kSoftThreads);
-        }
+        mbar_init(bar(C::kBarQFull), 1);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
             mbar_init(bar(C::kBarKEmpty + s), 1);
@@ -357,12 +341,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                     else itm = decode(k);
                 }
             };
+            // (One item per block: its Q tile loads once, into the one buffer.)
             auto load_q = [&](const Item &itm) -> bool {
                 const int qb = n_q % C::kQBufs;
-                // The buffer's previous item must have stored its output.
-                if (n_q >= C::kQBufs &&
-                    !mbar_wait(bar(C::kBarQEmpty + qb), ((n_q / C::kQBufs) - 1) & 1, ac))
-                    return false;
                 mbar_arrive_expect_tx(bar(C::kBarQFull + qb), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sb + C::kOffQ + qb * C::kTileBytes + c * C::kChunkBytes, &tmQ,
@@ -376,16 +357,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 if (t >= C::kKStages &&
                     !mbar_wait(bar(C::kBarKEmpty + ks), ((t / C::kKStages) - 1) & 1, ac))
                     return false;
-                // (Injected fault: block 0 never loads its first K tile; the
-                // tile still counts as issued, so the abort path's drain waits
-                // for it, with its own short limit.)
-                if (!(p.inject_skip_k0 && blockIdx.x == 0 && t == 0)) {
-                    mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
-                                    &tmK, bar(C::kBarKFull + ks), c * 64,
-                                    (ki.kv_lo + kj) * kBlockN, ki.bh_kv);
-                }
+                mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sb + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &tmK,
+                                bar(C::kBarKFull + ks), c * 64, (ki.kv_lo + kj) * kBlockN,
+                                ki.bh_kv);
                 k_issued = t + 1;
                 advance(kr, kj, ki, k_done);
                 return true;
@@ -582,29 +558,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tma_store_wait_read();
         }
         __syncwarp();
-    } else if (fwd_persistent<EXT>() && warp == kWarpOStore) {
-        // ------------------------------------------------ output storer
-        // Stores each item's output tile (staged by the softmax warpgroups in
-        // the item's Q buffer) and hands the buffer back to the producer once
-        // the store has read it.
-        if (lane == 0) {
-            for (int rnd = 0;; ++rnd) {
-                const int k = item_at(rnd);
-                if (k < 0) break;
-                const Item itm = decode(k);
-                const int qb = rnd % C::kQBufs;
-                if (!mbar_wait(bar(C::kBarOStaged + qb), (rnd / C::kQBufs) & 1, ac)) break;
-                if (*abort_flag == 0) {
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_store_3d(&tmO, sb + C::kOffQ + qb * C::kTileBytes + c * C::kChunkBytes,
-                                     c * 64, itm.row_lo, itm.bh);
-                    tma_store_commit();
-                    tma_store_wait_read();
-                }
-                mbar_arrive(bar(C::kBarQEmpty + qb));
-            }
-        }
-        __syncwarp();
     } else {
         // ---------------------------------------------- softmax warpgroups
         // Warpgroup wg handles keys [64 wg, 64 wg + 64) of every key tile for
@@ -639,13 +592,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const bool ragged = key0 + kBlockN > p.N;
             // Some row of the tile drops keys below its window start.
             const bool wedge = CAUSAL && p.window > 0 && key0 < row_lo + kBlockM - p.window;
-            // x ends up holding values whose row max commutes with a positive
-            // factor `xmul` that turns them into log2-unit logits t; xmul then
-            // folds into the exp2 FMA.  No residual: x is raw q.k and xmul the
-            // scale (in log2 units) when that is positive, else x is turned
-            // into t here.  Residual: x is the natural-unit logit y and xmul
-            // log2(e).
-            float xmul = kLog2e;
+            // x ends up holding the natural-unit logits y = scale q.k + bias,
+            // whose row max commutes with the factor xmul = log2(e) that turns
+            // them into log2-unit logits; xmul folds into the exp2 FMA.
+            const float xmul = kLog2e;
             float x[kHalfN];
             float mt_x = -INFINITY;
             bool got = ok && mbar_wait_warp(bar(C::kBarSFull + sbuf), (t >> 1) & 1, ac);
@@ -712,13 +662,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                         if (brow && inside) bval = __ldg(brow + c);
                         x[c] = fmaf(x[c], p.scale, bval);
                         if (erow && inside) erow[c] = x[c];
-                    }
-                } else {
-                    xmul = p.scale_log2;
-                    if (!(p.scale_log2 > 0.f)) {
-#pragma unroll
-                        for (int c = 0; c < kHalfN; ++c) x[c] *= p.scale_log2;
-                        xmul = 1.f;
                     }
                 }
 
@@ -837,15 +780,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             ok = false;
             break;
         }
-        if constexpr (fwd_persistent<EXT>()) {
-            mbar_arrive(bar(C::kBarOStaged + rnd % C::kQBufs));   // the storer warp takes it from here
-        } else {
-            if (threadIdx.x == 0 && *abort_flag == 0) {
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_store_3d(&tmO, o_tile + c * C::kChunkBytes, c * 64, row_lo, bh);
-                tma_store_commit();
-                tma_store_wait_read();
-            }
+        if (threadIdx.x == 0 && *abort_flag == 0) {
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_store_3d(&tmO, o_tile + c * C::kChunkBytes, c * 64, row_lo, bh);
+            tma_store_commit();
+            tma_store_wait_read();
         }
         }   // items
     }
@@ -878,8 +817,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_c(int ext, const FwdMaps &m, const FwdParams &prm, unsigned grid,
                      cudaStream_t stream) {
     if (ext == 2) return launch_t<D, CAUSAL, 2>(m, prm, grid, stream);
-    if (ext == 1) return launch_t<D, CAUSAL, 1>(m, prm, grid, stream);
-    return launch_t<D, CAUSAL, 0>(m, prm, grid, stream);
+    return launch_t<D, CAUSAL, 1>(m, prm, grid, stream);
 }
 
 template <int D>
@@ -917,7 +855,6 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
     prm.scale_log2 = pb.scale * kLog2e;
     prm.window = pb.causal ? pb.window : 0;
     prm.wait_limit_ns = pb.wait_limit_ns ? pb.wait_limit_ns : kWaitLimitNs;
-    prm.inject_skip_k0 = pb.inject_skip_k0;
     const long long n_items = static_cast<long long>(prm.n_qtiles) * BH;
     // Causal item order: one chunk of all heads unless their K/V is over
     // twice the L2; then chunks whose K/V is about half the L2, so that the
@@ -935,8 +872,8 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
             prm.hchunk = static_cast<int>(
                 std::max<long long>(1, std::min<long long>(BH, static_cast<long long>(0.5 * l2 / head_kv))));
     }
-    int ext = 0;
-    if (pb.bias || pb.emit) {
+    int ext = 1;
+    {
         // The staged variant maps the [N, N] planes as tensors of 128 x 32
         // fp32 boxes: rows must be 16-byte multiples, bases 16-byte aligned.
         const auto a16 = [](const void *ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
@@ -949,11 +886,8 @@ cudaError_t launch_fwd(const FwdProblem &pb, int *status, cudaStream_t stream) {
             ext = 1;
     }
     if (ext != 2) m.bias = m.emit = m.q;   // unused by the kernel
-    // The plain forward runs one persistent block per SM (each holds most of
-    // an SM's shared memory and all of its TMEM); the residual variants one
-    // block per (query tile, head).
-    unsigned grid = static_cast<unsigned>(n_items);
-    if (ext == 0 && n_items > di.sms) grid = static_cast<unsigned>(di.sms);
+    // One block per (query tile, head).
+    const unsigned grid = static_cast<unsigned>(n_items);
     switch (pb.D) {
     case 64: return launch_d<64>(pb.causal, ext, m, prm, grid, stream);
     case 80: return launch_d<80>(pb.causal, ext, m, prm, grid, stream);
