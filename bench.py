@@ -356,6 +356,10 @@ EXTRA_WORKLOADS = {
                                       D=128, causal=True),
     "profile_decode_small": dict(name="decode_B4_H32_KV8_N16384_D128", kind="decode", B=4,
                                  Hq=32, Hkv=8, N=16384, D=128, causal=True),
+    # One plain layer of the residual chain's shape (no bias, no emitted logits),
+    # forward + backward: what the residual adds is measured against it.
+    "gqa_fwd_bwd": dict(name="causal_fwd_bwd_B1_H20_KV4_N4096_D128", B=1, Hq=20, Hkv=4, N=4096,
+                        D=128, causal=True),
     # Causal sliding window of 4096 keys on the default step's shape.
     "swa_fwd_bwd": dict(name="swa4096_fwd_bwd_B1_H16_N16384_D128", B=1, Hq=16, Hkv=16, N=16384,
                         D=128, causal=True, window=4096),
