@@ -292,6 +292,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int res_bias = RES && p.has_bias ? kResChunks : 0;
     const int res_grad = RES && (p.has_gin || p.has_gout) ? kResChunks : 0;
     const int res_per_item = res_bias + res_grad;
+    // Within the bias (and the gradient) chunks of an item, position pos
+    // holds chunk 2 (pos % 2) + pos / 2, i.e. the order 0, 2, 1, 3: the
+    // first-half chunks of both P/dS warpgroups (chunk 2w + h is warpgroup
+    // w's query columns 32h..32h+31) come first.  A warpgroup hands its
+    // first bias chunk back halfway through its P phase, so the first
+    // gradient chunks can load while the P phase still runs.
+    auto res_chunk_at = [](int pos) { return 2 * (pos & 1) + (pos >> 1); };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -304,8 +311,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         for (int s = 0; s < C::kNumResSlots; ++s) {
             mbar_init(bar(C::kBarResFull + s), 1);
-            mbar_init(bar(C::kBarResDone + s), kTile);   // one P/dS warpgroup per chunk
-            mbar_init(bar(C::kBarResFree + s), 1);
+            // Done: the P/dS warpgroup that wrote a gradient chunk.  Free:
+            // the warpgroup that read a bias chunk, or the storer (one
+            // arrival of kTile) once a gradient chunk's store has read it.
+            mbar_init(bar(C::kBarResDone + s), kTile);
+            mbar_init(bar(C::kBarResFree + s), kTile);
         }
         mbar_init(bar(C::kBarSFull), 1);
         mbar_init(bar(C::kBarDPFull), 1);
@@ -347,8 +357,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (j >= C::kQStages && !(ok = mbar_wait(bar(C::kBarQEmpty + s), ph, ac))) break;
                 const int qi = item_qi(j), bhq = item_bhq(j);
                 const uint32_t fb = bar(C::kBarQFull + s);
-                // Q and the rows (and dO with one stage) on QFull, dO on DOFull
-                mbar_arrive_expect_tx(fb, (RES ? 2 : 1) * C::kTileBytes + 2 * kTile * 4);
+                // Q and the rows on QFull, dO on DOFull (so that S^T can
+                // start before dO has landed)
+                mbar_arrive_expect_tx(fb, C::kTileBytes + 2 * kTile * 4);
                 const uint32_t st = sb + C::kOffStage + s * C::kStageBytes;
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(st + c * C::kChunkBytes, &tmQ, fb, c * 64, qi * kTile, bhq);
@@ -360,8 +371,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (j >= C::kQStages && !(ok = mbar_wait(bar(C::kBarDOEmpty + s), ph, ac)))
                         break;
                 }
-                const uint32_t db = RES ? fb : bar(C::kBarDOFull + s);
-                if constexpr (!RES) mbar_arrive_expect_tx(db, C::kTileBytes);
+                // (With one stage dO's buffer goes back with Q's, on QEmpty.)
+                const uint32_t db = bar(C::kBarDOFull + s);
+                mbar_arrive_expect_tx(db, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tmdO, db, c * 64,
                                 qi * kTile, bhq);
@@ -372,10 +384,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 drain_wait(bar(C::kBarKV), 0);
                 for (int j = max(issued - C::kQStages, 0); j < issued; ++j)
                     drain_wait(bar(C::kBarQFull + j % C::kQStages), (j / C::kQStages) & 1);
-                if constexpr (!RES) {
-                    for (int j = max(issued_do - C::kQStages, 0); j < issued_do; ++j)
-                        drain_wait(bar(C::kBarDOFull + j % C::kQStages), (j / C::kQStages) & 1);
-                }
+                for (int j = max(issued_do - C::kQStages, 0); j < issued_do; ++j)
+                    drain_wait(bar(C::kBarDOFull + j % C::kQStages), (j / C::kQStages) & 1);
             }
         }
         __syncwarp();
@@ -389,7 +399,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             auto stage_of = [&](int j) -> uint32_t {
                 return sb + C::kOffStage + (j % C::kQStages) * C::kStageBytes;
             };
-            auto wait_stage = [&](int j) -> bool {   // Q (and dO with one stage)
+            auto wait_stage = [&](int j) -> bool {   // Q and the LSE / Delta rows
                 if (!mbar_wait(bar(C::kBarQFull + j % C::kQStages), (j / C::kQStages) & 1, ac))
                     return false;
                 tc_fence_after();
@@ -468,6 +478,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (!(ok = wait_stage(j))) break;
                     issue_st(j);
                     if (j > 0 && !(ok = wait_on(C::kBarDQEmpty, j - 1))) break;
+                    if (!(ok = wait_do(j))) break;
                     issue_dpt(j);
                     if (!(ok = wait_on(C::kBarPReady, j))) break;
                     issue_dv(j);
@@ -512,6 +523,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // Bias and incoming-gradient chunks by TMA (zero fill past N); a
         // gradient chunk with no incoming gradient is only handed over.
         if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();   // each chunk is read once
             bool ok = true;
             int slot = 0, issued = 0, gi = 0;
             uint32_t phase = 0;
@@ -521,15 +533,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (gi >= kResSlots) ok = mbar_wait(bar(C::kBarResFree + slot), phase ^ 1u, ac);
                     if (!ok) break;
                     const bool is_bias = idx < res_bias;
-                    const int c = is_bias ? idx : idx - res_bias;
+                    const int c = res_chunk_at(is_bias ? idx : idx - res_bias);
                     const uint32_t full = bar(C::kBarResFull + slot);
                     const CUtensorMap *map = is_bias ? &tmBias : (p.has_gin ? &tmGin : nullptr);
                     if (map) {
                         mbar_arrive_expect_tx(full, kResChunkBytes);
                         for (int bx = 0; bx < kTile / kResQ; ++bx)
-                            tma_load_3d(sb + C::kOffRes + slot * kResChunkBytes + bx * (kResQ * 128),
-                                        map, full, kt * kTile + bx * kResQ, qi * kTile + c * kResQ,
-                                        bhq);
+                            tma_load_3d_hint(sb + C::kOffRes + slot * kResChunkBytes +
+                                                 bx * (kResQ * 128),
+                                             map, full, kt * kTile + bx * kResQ,
+                                             qi * kTile + c * kResQ, bhq, pol);
                     } else {
                         mbar_arrive(full);
                     }
@@ -546,25 +559,33 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (RES && warp == 15) {
         // ---------------------------------- outgoing logit-gradient storer
-        if (lane == 0) {
+        // Gradient chunks only (bias chunks go back to the loader straight
+        // from the warpgroup that read them): wait until the chunk is
+        // written, store it (when an outgoing gradient is wanted), and hand
+        // the slot back once the store has read it.  The chunk sequence of
+        // an item puts its gradient chunks in slots 0..3 (after the bias
+        // chunks in 0..3, if any), so each slot's Done barrier completes once
+        // per item.
+        if (lane == 0 && res_grad) {
+            const uint64_t pol = l2_policy_evict_first();   // written once
             bool ok = true;
-            int slot = 0;
-            uint32_t phase = 0;
             for (int j = 0; j < n_items && ok; ++j) {
                 const int qi = item_qi(j), bhq = item_bhq(j);
-                for (int idx = 0; idx < res_per_item; ++idx) {
-                    if (!(ok = mbar_wait(bar(C::kBarResDone + slot), phase, ac))) break;
-                    if (idx >= res_bias && p.has_gout) {
-                        const int c = idx - res_bias;
+                for (int pos = 0; pos < kResChunks; ++pos) {
+                    const int c = res_chunk_at(pos);
+                    const int slot = (j * res_per_item + res_bias + pos) % kResSlots;
+                    if (!(ok = mbar_wait(bar(C::kBarResDone + slot), j & 1, ac))) break;
+                    if (p.has_gout) {
                         for (int bx = 0; bx < kTile / kResQ; ++bx)
-                            tma_store_3d(&tmGout,
-                                         sb + C::kOffRes + slot * kResChunkBytes + bx * (kResQ * 128),
-                                         kt * kTile + bx * kResQ, qi * kTile + c * kResQ, bhq);
+                            tma_store_3d_hint(&tmGout,
+                                              sb + C::kOffRes + slot * kResChunkBytes +
+                                                  bx * (kResQ * 128),
+                                              kt * kTile + bx * kResQ, qi * kTile + c * kResQ, bhq,
+                                              pol);
                         tma_store_commit();
                         tma_store_wait_read();
                     }
-                    mbar_arrive(bar(C::kBarResFree + slot));
-                    if (++slot == kResSlots) { slot = 0; phase ^= 1u; }
+                    mbar_arrive_n(bar(C::kBarResFree + slot), kTile);
                 }
             }
             tma_store_wait_read();
@@ -745,7 +766,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if constexpr (RES) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int gb = j * res_per_item + 2 * w + h;
+                    const int gb = j * res_per_item + 2 * h + w;   // position of chunk 2w + h
                     const int gg = gb + res_bias;
                     bsi[h] = gb % kResSlots;
                     gsi[h] = gg % kResSlots;
@@ -791,14 +812,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         }
                         pw[(c + u) >> 1] = pack_bf16x2(p0, p1);
                     }
+                    if constexpr (RES) {
+                        // First bias chunk (columns 0..31) read: back to the loader.
+                        if (c == kResQ - 4 && res_bias) mbar_arrive(bar(C::kBarResFree + bsi[0]));
+                    }
                 }
             }
             tmem_st32(tS, pw);   // columns 64w..64w+31, already read
             if constexpr (RES) {
-                if (res_bias) {   // bias chunks read: hand them back
-                    mbar_arrive(bar(C::kBarResDone + bsi[0]));
-                    mbar_arrive(bar(C::kBarResDone + bsi[1]));
-                }
+                if (res_bias) mbar_arrive(bar(C::kBarResFree + bsi[1]));   // second bias chunk
             }
             tmem_st_wait();
             tc_fence_before();
@@ -814,7 +836,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if constexpr (RES) {
                     if (res_grad && !mbar_wait_warp(bar(C::kBarResFull + gsi[h]),
                                                     static_cast<uint32_t>(
-                                                        (j * res_per_item + res_bias + 2 * w + h) /
+                                                        (j * res_per_item + res_bias + 2 * h + w) /
                                                         kResSlots) & 1u,
                                                     ac)) {
                         ok = false;
