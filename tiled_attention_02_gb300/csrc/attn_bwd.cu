@@ -145,7 +145,11 @@ struct BwdCfg {
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kDQBoxes = (D + 31) / 32;   // fp32 dQ boxes of 32 columns
     // The residual variant keeps one {Q, dO} stage and gives the other's
-    // shared memory to its fp32 chunk ring.
+    // shared memory to its fp32 chunk ring.  Its stage's two tile buffers
+    // swap roles every item: Q(j) in buffer j % 2, dO(j) in buffer
+    // (j + 1) % 2.  dO(j) is last read by dV(j), well before Q(j) is last
+    // read by dK(j), so Q(j + 1) loads into dO(j)'s buffer while item j's
+    // dS work runs, and dO(j + 1) into Q(j)'s buffer after dK(j).
     static constexpr int kQStages = RES ? 1 : 2;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTileBytes;
@@ -163,7 +167,7 @@ struct BwdCfg {
     // in the one-stage residual variant); DOFull / DOEmpty cover dO (two-stage
     // variant), whose buffer also stages part of dQ.
     static constexpr int kBarQFull = 1;      // 2
-    static constexpr int kBarQEmpty = 3;     // 2
+    static constexpr int kBarQEmpty = 3;     // 2 (residual variant: per tile buffer)
     static constexpr int kBarSFull = 5;
     static constexpr int kBarDPFull = 6;
     static constexpr int kBarPReady = 7;
@@ -351,7 +355,35 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                             kt * kTile, bh_kv);
             }
             int issued = 0, issued_do = 0;
-            for (int j = 0; j < n_items; ++j) {
+            if constexpr (RES) {
+                // Q(j) and the rows into buffer / row slot j % 2 once dO(j - 1)
+                // (the buffer's previous use) is done; dO(j) into buffer
+                // (j + 1) % 2 once Q(j - 1) is done.  Each buffer is used once
+                // per item, so its empty barrier completes phase j at item j.
+                for (int j = 0; j < n_items; ++j) {
+                    const int qi = item_qi(j), bhq = item_bhq(j);
+                    const int bq = j & 1, bd = bq ^ 1;
+                    const uint32_t ph = static_cast<uint32_t>(j - 1) & 1u;
+                    if (j > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty + bq), ph, ac))) break;
+                    const uint32_t fb = bar(C::kBarQFull);
+                    mbar_arrive_expect_tx(fb, C::kTileBytes + 2 * kTile * 4);
+                    const uint32_t sq = sb + C::kOffStage + bq * C::kTileBytes;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sq + c * C::kChunkBytes, &tmQ, fb, c * 64, qi * kTile, bhq);
+                    const size_t prow = static_cast<size_t>(bhq) * p.NP + qi * kTile;
+                    bulk_load(s_rows + bq * kTile * 4, p.lse2 + prow, kTile * 4, fb);
+                    bulk_load(s_rows + (2 + bq) * kTile * 4, p.delta + prow, kTile * 4, fb);
+                    issued = j + 1;
+                    if (j > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty + bd), ph, ac))) break;
+                    const uint32_t db = bar(C::kBarDOFull);
+                    mbar_arrive_expect_tx(db, C::kTileBytes);
+                    const uint32_t sd = sb + C::kOffStage + bd * C::kTileBytes;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sd + c * C::kChunkBytes, &tmdO, db, c * 64, qi * kTile, bhq);
+                    issued_do = j + 1;
+                }
+            }
+            for (int j = 0; j < (RES ? 0 : n_items); ++j) {
                 const int s = j % C::kQStages;
                 const uint32_t ph = ((j / C::kQStages) - 1) & 1;
                 if (j >= C::kQStages && !(ok = mbar_wait(bar(C::kBarQEmpty + s), ph, ac))) break;
@@ -381,6 +413,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 issued_do = j + 1;
             }
             if (!ok) {
+                // (Residual variant: one Q and one dO load in flight at most,
+                // on barrier 0 of each.)
                 drain_wait(bar(C::kBarKV), 0);
                 for (int j = max(issued - C::kQStages, 0); j < issued; ++j)
                     drain_wait(bar(C::kBarQFull + j % C::kQStages), (j / C::kQStages) & 1);
@@ -398,6 +432,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV, sDS = sb + C::kOffDS;
             auto stage_of = [&](int j) -> uint32_t {
                 return sb + C::kOffStage + (j % C::kQStages) * C::kStageBytes;
+            };
+            // Q(j) and dO(j) tiles (the residual variant alternates buffers).
+            auto q_of = [&](int j) -> uint32_t {
+                return RES ? sb + C::kOffStage + (j & 1) * C::kTileBytes : stage_of(j);
+            };
+            auto do_of = [&](int j) -> uint32_t {
+                return RES ? sb + C::kOffStage + ((j + 1) & 1) * C::kTileBytes
+                           : stage_of(j) + C::kTileBytes;
             };
             auto wait_stage = [&](int j) -> bool {   // Q and the LSE / Delta rows
                 if (!mbar_wait(bar(C::kBarQFull + j % C::kQStages), (j / C::kQStages) & 1, ac))
@@ -417,7 +459,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 return true;
             };
             auto issue_st = [&](int j) {   // S^T = K Q^T (over P^T(j-1), read by dV(j-1))
-                const uint32_t sQ = stage_of(j);
+                const uint32_t sQ = q_of(j);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -427,7 +469,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mma_commit(bar(C::kBarSFull));
             };
             auto issue_dpt = [&](int j) {   // dP^T = V dO^T (over dQ(j-1), drained)
-                const uint32_t sdO = stage_of(j) + C::kTileBytes;
+                const uint32_t sdO = do_of(j);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -437,7 +479,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mma_commit(bar(C::kBarDPFull));
             };
             auto issue_dv = [&](int j) {   // dV += P^T dO  (A in TMEM)
-                const uint32_t sdO = stage_of(j) + C::kTileBytes;
+                const uint32_t sdO = do_of(j);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     // P^T of query columns 64w..64w+63 sits in TMEM columns
@@ -446,9 +488,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                            sdesc_sw128(sdO + kk * 2048, C::kChunkBytes, 1024), kIdAcc,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
+                // Residual variant: dO(j)'s buffer is free (Q(j + 1) loads there).
+                if (RES) mma_commit(bar(C::kBarQEmpty + ((j + 1) & 1)));
             };
             auto issue_dk_dq = [&](int j) {   // dK += dS^T Q, then dQ = dS K (over dP^T(j), read)
-                const uint32_t sQ = stage_of(j);
+                const uint32_t sQ = q_of(j);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -464,10 +508,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 mma_commit(bar(C::kBarDQFull));   // also: every MMA of item j has completed
                 mma_commit(bar(C::kBarDSFree));
-                // Q (and, with one stage, dO) of the item are free now; with two
-                // stages the drain hands dO's buffer back once its reductions
-                // have read the part of dQ staged there.
-                mma_commit(bar(C::kBarQEmpty + j % C::kQStages));
+                // Q of the item is free now (residual variant: Q(j)'s buffer,
+                // where dO(j + 1) loads); with two stages the drain hands dO's
+                // buffer back once its reductions have read the part of dQ
+                // staged there.
+                mma_commit(bar(C::kBarQEmpty + (RES ? (j & 1) : j % C::kQStages)));
             };
             bool ok = mbar_wait(bar(C::kBarKV), 0, ac);
             if constexpr (RES) {
@@ -756,8 +801,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // Some query column of the tile lies W or more rows past some key row.
             const int qoff = (item_qi(j) - kt) * kTile;   // query row - key row offset of the tiles
             const bool wedge = CAUSAL && p.window > 0 && qoff + kTile - 1 >= p.window;
-            const uint32_t s_lse = s_rows + s * kTile * 4 + w * 256;
-            const uint32_t s_dlt = s_rows + (2 + s) * kTile * 4 + w * 256;
+            const int rs = RES ? (j & 1) : s;   // row slot (the residual variant alternates)
+            const uint32_t s_lse = s_rows + rs * kTile * 4 + w * 256;
+            const uint32_t s_dlt = s_rows + (2 + rs) * kTile * 4 + w * 256;
             uint32_t pw[32];   // P^T of this warpgroup's 64 columns, bf16 pairs
             // Residual chunks of this warpgroup: query columns 64w + 32h .. +31
             // are chunk 2w + h of the bias and of the logit gradient.
