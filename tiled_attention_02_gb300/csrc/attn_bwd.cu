@@ -1137,9 +1137,14 @@ cudaError_t launch_d(const BwdProblem &pb, int *status, cudaStream_t stream) {
     const double acc_bytes = static_cast<double>(BH) * pb.N * D * 4.0;
     const double head_bytes = static_cast<double>(prm.group) * pb.N * D * 4.0;   // per kv head
     prm.hchunk = static_cast<int>(BHkv);
-    if (acc_bytes > 2.0 * l2) {
+    // Chunked once the accumulator is over half the L2: a chunk's
+    // accumulator takes a quarter of it, beside the chunk's Q and dO (as
+    // large again in bf16), so that its reduce-adds stay in L2.  (Measured at
+    // B1 H16 N16384 D128: DRAM traffic 2.9 GB -> 0.66 GB, 1.2x the
+    // algorithmic bytes, time +1%; at B4 H32 N4096 D128: 22% faster.)
+    if (acc_bytes > 0.5 * l2) {
         // (a divisor of the kv head count: every chunk is whole)
-        long long hc = std::max<long long>(1, std::min<long long>(BHkv, static_cast<long long>(0.5 * l2 / head_bytes)));
+        long long hc = std::max<long long>(1, std::min<long long>(BHkv, static_cast<long long>(0.25 * l2 / head_bytes)));
         while (BHkv % hc != 0) --hc;
         // The chunks are gridDim.y (at most 65535); a head count with no
         // divisor near the target keeps the plain order.
