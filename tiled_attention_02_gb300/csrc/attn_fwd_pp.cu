@@ -660,7 +660,13 @@ fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const bool diag = CAUSAL && (j == qt);
                 const bool ragged = key0 + kBlockN > p.N;
                 const bool wedge = CAUSAL && p.window > 0 && key0 < row_lo + kBlockM - p.window;
-                if (diag || ragged || wedge) {
+                if (diag && !ragged && !wedge) {
+                    // The diagonal tile alone: key c kept iff c <= r (one
+                    // compare per key; the general form below is several
+                    // times slower and sits on every item's last tile).
+#pragma unroll
+                    for (int c = 0; c < kBlockN; ++c) x[c] = c <= r ? x[c] : -INFINITY;
+                } else if (diag || ragged || wedge) {
                     const int klo = wedge ? q_row - p.window + 1 - key0 : -(1 << 30);
                     const int khi = diag ? r : (1 << 30);          // last kept key (causal)
                     const int kend = p.N - key0;                    // keys past N
