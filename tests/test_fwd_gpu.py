@@ -141,6 +141,34 @@ def test_parity_full_size_sampled(ta, orc, name, B, Hq, Hkv, N, D, causal):
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
 
 
+# Rows of 64 key tiles or more take the variant whose K and V tiles share
+# one stage ring (D >= 80; D = 64 always does): both sides of the threshold,
+# ragged, causal and not, grouped heads, every head dim the variant has.
+MERGE_EDGE = [
+    # B, Hq, Hkv, N, D, causal
+    (1, 4, 2, 8063, 128, True),    # 63 key tiles: separate K and V rings
+    (1, 4, 2, 8065, 128, True),    # 64 key tiles, the last ragged: merged
+    (1, 3, 3, 8192 + 37, 96, False),
+    (1, 2, 1, 9000, 80, True),
+]
+
+
+@pytest.mark.parametrize("case", MERGE_EDGE,
+                         ids=[f"B{c[0]}H{c[1]}kv{c[2]}N{c[3]}D{c[4]}{'c' if c[5] else 'nc'}"
+                              for c in MERGE_EDGE])
+def test_parity_merged_kv_stages(ta, orc, case):
+    B, Hq, Hkv, N, D, causal = case
+    x = make_qkv(B, Hq, Hkv, N, D, seed=7)
+    o, lse = run_fwd(ta, x, causal=causal)
+    rows = np.unique(np.concatenate([sample_rows(B, Hq, N, 160, seed=8),
+                                     [0, N - 1, N - 128, B * Hq * N - 1]]))
+    ref = oracle_fwd(orc, x, causal, 1 / math.sqrt(D), rows=rows)
+    name = f"N={N} D={D} causal={causal}"
+    check_o(o.reshape(-1, D)[torch.from_numpy(rows).cuda()], ref["o"], name)
+    check_lse(lse.reshape(-1)[torch.from_numpy(rows).cuda()], ref["lse"], name)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
 # More (query tile, head) items than SMs, so that the plain forward's
 # persistent blocks each walk several items (the rings, S/P buffers and output
 # buffers continue across item boundaries), with a ragged last tile, grouped
